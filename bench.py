@@ -1,0 +1,551 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache hot path on one GB300.
+
+One step = one decode step of a Qwen3-0.6B-shaped model over a batch of 256
+sequences with contexts uniform in [1024, 8192] tokens and all 28 layers'
+KV caches resident in HBM (separate per-layer pools, block size 256): for
+each layer, kv_store of the step's new token then paged decode attention.
+Inputs total ~139 GB, far larger than L2, so no flush is needed between steps.
+
+Printed (one JSON line, rank 0):
+  value       algorithmic HBM bytes of the whole step (store + decode, 28 layers) / step time, GB/s
+  roofline    the dominant kernel (paged decode) against the measured HBM copy peak
+  e2e         the same metric through the public API with host buffers (H2D inputs, D2H outputs)
+  prefill     the varlen prefill row on a 16-sequence prefix-cached chunked batch, TFLOP/s
+  cpu_baseline the CPU oracle timed on a bounded sample of the same workload
+
+``--impl reference`` times the CPU oracle itself on bounded samples of the
+same workload (there is no other reference implementation of this path).
+"""
+
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")  # the CPU oracle runs on one core; its line says so
+
+import argparse
+import hashlib
+import json
+import math
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn HBM GB/s"
+UNIT = "GB/s"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks and clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        sel = self._selector(device_index)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"] + sel, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    @staticmethod
+    def _selector(device_index: int):
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            bus = getattr(props, "pci_bus_id", None)
+            dom = getattr(props, "pci_domain_id", 0)
+            dev = getattr(props, "pci_device_id", 0)
+            if bus is not None:
+                return ["-i", f"{dom:08x}:{bus:02x}:{dev:02x}.0"]
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return ["-i", vis.split(",")[device_index]]
+        return ["-i", str(device_index)]
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def decode_traffic_record():
+    """ncu DRAM bytes per decode launch, valid only for the decode source it was taken on."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_qwen3_b256_traffic.md")
+    src = os.path.join(ROOT, "pagedattention_kv_cache_gb300", "csrc", "decode.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"decode\.cu sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram bytes per full launch:\s*([0-9]+)", text)
+    if not m_sha or not m_b:
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return int(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def decode_alg_bytes(w) -> int:
+    elt = torch.finfo(w.dtype).bits // 8
+    kv = sum(w.context_lens) * w.num_kv_heads * w.head_dim * 2 * elt
+    qo = 2 * w.batch * w.num_q_heads * w.head_dim * elt
+    meta = sum(-(-n // w.block_size) for n in w.context_lens) * 4 + w.batch * 4
+    return kv + qo + meta
+
+
+def store_alg_bytes(n_tokens: int, w) -> int:
+    elt = torch.finfo(w.dtype).bits // 8
+    return 2 * 2 * n_tokens * w.num_kv_heads * w.head_dim * elt + 4 * n_tokens
+
+
+def prefill_flops(p) -> int:
+    total = 0
+    for c, n in zip(p.num_cached, p.num_new):
+        total += n * c + n * (n + 1) // 2  # sum over rows r < n of (c + r + 1) keys
+    return 4 * p.head_dim * p.num_q_heads * total
+
+
+def prefill_alg_bytes(p) -> int:
+    elt = 2
+    q = sum(p.num_new) * p.num_q_heads * p.head_dim * elt
+    kv = sum(c + n for c, n in zip(p.num_cached, p.num_new)) * p.num_kv_heads * p.head_dim * 2 * elt
+    return 2 * q + kv
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class DecodeState:
+    def __init__(self, w, device):
+        import pagedattention_kv_cache_gb300 as pkv
+        from pagedattention_kv_cache_gb300 import metadata as md
+        from pagedattention_kv_cache_gb300 import workloads as wl
+
+        self.pkv = pkv
+        self.w = w
+        L = w.num_layers
+        elt = torch.finfo(w.dtype).bits // 8
+        need = 2 * L * w.num_blocks * w.block_size * w.num_kv_heads * w.head_dim * elt
+        free, _ = torch.cuda.mem_get_info(device)
+        if need + (8 << 30) > free:
+            raise RuntimeError(f"workload needs {need / 1e9:.1f} GB of KV cache; {free / 1e9:.1f} GB free")
+        self.k_cache, self.v_cache, self.q, self.k_new, self.v_new = [], [], [], [], []
+        for layer in range(L):
+            t = wl.decode_tensors(w, device, layer=layer)
+            self.k_cache.append(t["k_cache"])
+            self.v_cache.append(t["v_cache"])
+            self.q.append(t["q"])
+            self.k_new.append(t["k_new"])
+            self.v_new.append(t["v_new"])
+            del t
+        meta = md.decode_metadata(w.block_tables, w.context_lens, w.block_size)
+        self.meta_host = meta
+        self.meta = md.to_device(meta, device)
+        self.out = [torch.empty_like(q) for q in self.q]
+        self.ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0, device=device)
+
+    def step(self, events=None, q=None, k_new=None, v_new=None, meta=None, out=None):
+        pkv = self.pkv
+        q = q or self.q
+        k_new = k_new or self.k_new
+        v_new = v_new or self.v_new
+        meta = meta or self.meta
+        out = out or self.out
+        for layer in range(self.w.num_layers):
+            pkv.kv_store(k_new[layer], v_new[layer], self.k_cache[layer], self.v_cache[layer], meta["slot_mapping"])
+            if events is not None:
+                events[layer][0].record()
+            pkv.paged_decode_attn(q[layer], self.k_cache[layer], self.v_cache[layer], meta["block_tables"],
+                                  meta["context_lens"], self.w.scale, workspace=self.ws, out=out[layer])
+            if events is not None:
+                events[layer][1].record()
+
+
+def bench_decode(args, device, world):
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b256_28l()
+    st = DecodeState(w, device)
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+
+    L = w.num_layers
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index or 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(args.steps):
+        st.step(events=ev[k])
+    stop.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = max_over_ranks(start.elapsed_time(stop), world, device)
+    decode_ms = [a.elapsed_time(b) for per in ev for (a, b) in per]
+    assert st.pkv.device_error() == 0
+
+    step_bytes = L * (decode_alg_bytes(w) + store_alg_bytes(w.batch, w))
+    ms_step = ms_total / args.steps
+    value = sum_over_ranks(step_bytes * args.steps, world, device) / (ms_total * 1e-3) / 1e9
+    return dict(w=w, st=st, ms_step=ms_step, value=value, decode_ms=decode_ms, clocks=clocks,
+                step_bytes=step_bytes, launches=2 * L * args.steps)
+
+
+def bench_e2e(args, res, device, world):
+    """Same step through the public API with pinned host inputs copied in and outputs copied out."""
+    st, w = res["st"], res["w"]
+    L = w.num_layers
+    h_q = [q.cpu().pin_memory() for q in st.q]
+    h_k = [k.cpu().pin_memory() for k in st.k_new]
+    h_v = [v.cpu().pin_memory() for v in st.v_new]
+    h_meta = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in st.meta_host.items()}
+    h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in st.out]
+    d_q = [torch.empty_like(q) for q in st.q]
+    d_k = [torch.empty_like(k) for k in st.k_new]
+    d_v = [torch.empty_like(v) for v in st.v_new]
+    d_meta = {k: torch.empty_like(v, device=device) for k, v in h_meta.items()}
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + list(h_meta.values()))
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for dst, src in zip(d_q + d_k + d_v, h_q + h_k + h_v):
+            dst.copy_(src, non_blocking=True)
+        for key in h_meta:
+            d_meta[key].copy_(h_meta[key], non_blocking=True)
+        st.step(q=d_q, k_new=d_k, v_new=d_v, meta=d_meta, out=st.out)
+        for dst, src in zip(h_out, st.out):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        one()
+    stop.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    ms = max_over_ranks(max(start.elapsed_time(stop), wall * 1e3), world, device)
+    value = sum_over_ranks(res["step_bytes"] * args.steps, world, device) / (ms * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / args.steps, 4)}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def bench_prefill(args, device):
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    p = wl.qwen3_prefill_prefix()
+    t = wl.prefill_tensors(p, device)
+    meta = md.prefill_metadata(p.block_tables, p.num_cached, p.num_new, p.block_size, always_tables=True)
+    gm = md.to_device(meta, device)
+    out = torch.empty_like(t["q"])
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(4 * l2 // 4, dtype=torch.float32, device=device)
+
+    def run():
+        pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], gm["slot_mapping"])
+        e0.record()
+        pkv.paged_varlen_prefill_attn(t["q"], gm["cu_seqlens_q"], gm["cu_seqlens_k"], meta["max_seqlen_q"],
+                                      meta["max_seqlen_k"], p.scale, k_cache=t["k_cache"], v_cache=t["v_cache"],
+                                      block_tables=gm["block_tables"], out=out)
+        e1.record()
+
+    times = []
+    reps = max(10, args.steps)
+    for i in range(args.warmup + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_l2(flush)
+        run()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    flops = prefill_flops(p)
+    return {"workload": p.name, "flops_per_call": flops, "ms_median": round(ms, 4), "ms_min": round(min(times), 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "reps": reps, "l2": "flushed before each rep",
+            "alg_bytes_per_call": prefill_alg_bytes(p)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_decode_sample(w, state=None, budget_s: float = 12.0, max_seqs: int = 64, seed: int = 0):
+    """Time the oracle's decode attention on whole sequences of layer 0 until ``budget_s`` elapses.
+
+    Returns (algorithmic bytes processed, seconds, sequences).  With a GPU
+    state the sequences' blocks are copied from the device pools; without,
+    the same-shaped blocks are drawn on the CPU.
+    """
+    from oracle import attention as oa
+
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.batch)[:max_seqs].tolist()
+    elt = torch.finfo(w.dtype).bits // 8
+    done_bytes, elapsed, nseq = 0, 0.0, 0
+    gen = torch.Generator().manual_seed(seed)
+    for b in order:
+        table = w.block_tables[b]
+        ctx = w.context_lens[b]
+        if state is not None:
+            idx = torch.tensor(table, device=state.k_cache[0].device)
+            kc = state.k_cache[0].index_select(0, idx).float().cpu().numpy()
+            vc = state.v_cache[0].index_select(0, idx).float().cpu().numpy()
+            q = state.q[0][b:b + 1].float().cpu().numpy()
+        else:
+            shape = (len(table), w.block_size, w.num_kv_heads, w.head_dim)
+            kc = torch.randn(shape, generator=gen).to(w.dtype).float().numpy()
+            vc = torch.randn(shape, generator=gen).to(w.dtype).float().numpy()
+            q = torch.randn((1, w.num_q_heads, w.head_dim), generator=gen).to(w.dtype).float().numpy()
+        local_table = np.arange(len(table), dtype=np.int32)[None, :]
+        t0 = time.perf_counter()
+        oa.paged_decode_attention(q, kc, vc, local_table, np.array([ctx]), w.scale)
+        elapsed += time.perf_counter() - t0
+        done_bytes += ctx * w.num_kv_heads * w.head_dim * 2 * elt + 2 * w.num_q_heads * w.head_dim * elt
+        nseq += 1
+        if elapsed >= budget_s:
+            break
+    return done_bytes, elapsed, nseq
+
+
+def cpu_baseline(w, state=None, budget_s: float = 12.0):
+    nbytes, secs, nseq = oracle_decode_sample(w, state, budget_s)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"float64 numpy oracle, layer 0 decode attention of {nseq} whole sequences of the same "
+                      f"batch ({nbytes / 1e6:.0f} MB of algorithmic bytes, {secs:.1f} s, one thread)"}
+
+
+def run_reference(args):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return 0
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b256_28l()
+    per_step_budget = 4.0
+    for k in range(args.warmup):
+        oracle_decode_sample(w, None, budget_s=0.5, max_seqs=1, seed=100 + k)
+    total_bytes, total_s = 0, 0.0
+    for k in range(args.steps):
+        b, s, _ = oracle_decode_sample(w, None, budget_s=per_step_budget, max_seqs=4, seed=k)
+        total_bytes += b
+        total_s += s
+    value = total_bytes / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": "up to 4 whole sequences of layer 0 per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "float64 numpy oracle, decode attention of up to 4 whole sequences per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    dist_init(world, local, "nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    hbm_peak, tc_peak, tc_sust, peak_src = measured_peaks()
+
+    res = bench_decode(args, device, world)
+    w = res["w"]
+    dec_ms = statistics.mean(res["decode_ms"])
+    dec_bytes = decode_alg_bytes(w)
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    e2e = bench_e2e(args, res, device, world)
+    prefill = bench_prefill(args, device)
+    prefill["roofline"] = {"bound": "tensor", "achieved": prefill["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+                           "frac": round(prefill["tflops"] / tc_peak, 4), "peak_source": f"{peak_src} bf16 burst"}
+    line = {
+        "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "layers": w.num_layers, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "context": "uniform [1024, 8192]", "kv_bytes_resident": 2 * w.num_layers * w.num_blocks *
+                   w.block_size * w.num_kv_heads * w.head_dim * 2, "l2": "inputs (~139 GB) larger than L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "decode_tokens_per_s": round(world * w.batch / (res["ms_step"] * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": decode_traffic_record(),
+                     "kernel": "paged_decode_kernel", "alg_bytes_per_launch": dec_bytes,
+                     "ms_per_launch": round(dec_ms, 5), "peak_source": f"{peak_src} HBM copy"},
+        "e2e": e2e,
+        "prefill": prefill,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, res["st"])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_profile_case(args):
+    """Small single-kernel cases for ncu captures (a few GB on the device, inputs larger than L2)."""
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if args.profile == "decode":
+        w = wl.qwen3_decode_b256_28l(batch=128, num_layers=1)
+        st = DecodeState(w, device)
+        for _ in range(3):
+            st.step()
+    elif args.profile == "decode-long":
+        w = wl.long_context_decode()
+        st = DecodeState(w, device)
+        for _ in range(3):
+            st.step()
+    elif args.profile == "prefill":
+        p = wl.qwen3_prefill_prefix()
+        t = wl.prefill_tensors(p, device)
+        meta = md.prefill_metadata(p.block_tables, p.num_cached, p.num_new, p.block_size, always_tables=True)
+        gm = md.to_device(meta, device)
+        for _ in range(3):
+            pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], gm["slot_mapping"])
+            pkv.paged_varlen_prefill_attn(t["q"], gm["cu_seqlens_q"], gm["cu_seqlens_k"], meta["max_seqlen_q"],
+                                          meta["max_seqlen_k"], p.scale, k_cache=t["k_cache"], v_cache=t["v_cache"],
+                                          block_tables=gm["block_tables"])
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    print(f"profile case {args.profile} done", flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "decode-long", "prefill"],
+                    help="run a small single-kernel case for ncu instead of the benchmark")
+    args = ap.parse_args()
+    if args.profile:
+        return run_profile_case(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV-cache attention library (libpagedkv.so).
+ *
+ * Three operations, each the kernel-level step named in "3.6 ModelRunner,
+ * CUDA Graph, and benchmarks" (a walk through nano-vllm's engine loop):
+ *
+ *   pkv_kv_store                  writes each new token's K/V row into its cache slot
+ *                                 (section 2, "Turning sequences into tensors": slot =
+ *                                 physical_block_id * block_size + offset_in_block;
+ *                                 section 5: slot -1 writes nothing)
+ *   pkv_paged_decode_attn         one query token per sequence, attention over
+ *                                 context_lens[b] cached tokens gathered through the
+ *                                 block table (section 2, decode; section 5, padding
+ *                                 rows with context_lens 0), split over the context with
+ *                                 a log-sum-exp combine
+ *   pkv_paged_varlen_prefill_attn packed variable-length (chunked) prefill with
+ *                                 cu_seqlens_q / cu_seqlens_k, reading prefix-cached
+ *                                 history through block_tables when K is longer than Q
+ *                                 (section 2, prepare_prefill)
+ *
+ * Attention is softmax(scale * q K^T) V per query head; query head h reads KV
+ * head h / (num_q_heads / num_kv_heads) (grouped-query attention, contiguous
+ * groups).  Call order is the caller's: store first, then attend, so the new
+ * token is part of its own context (section 2: context_lens counts it).
+ *
+ * Cache layout for one layer (section 4, "How KV Cache GPU memory is carved
+ * out"): k_cache and v_cache are each [num_blocks, block_size, num_kv_heads,
+ * head_dim], row-major and contiguous, in the element type given by `dtype`.
+ * A whole-model cache (2, layers, blocks, block_size, kv_heads, head_dim)
+ * is passed one layer slice at a time.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" must be device memory (or managed memory)
+ *    of the current CUDA device; the library dereferences them only on the
+ *    GPU.  Tensor pointers must be 16-byte aligned.
+ *  - The caller owns every buffer.  The library allocates no device memory.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *    nothing synchronises.  Argument errors are detected on the host and
+ *    returned as a negative pkv_status before anything is launched.
+ *  - Indices read on the device (slots, block ids, context lengths, cu_seqlens)
+ *    are range-checked by the kernels: an out-of-range value skips the access
+ *    and raises a bit in the per-device error word (pkv_get_device_error);
+ *    the kernels never trap.
+ *  - Element offsets are computed in 64-bit; counts are int32.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_F32 = 0,  /* float32 K/V/q/out */
+  PKV_BF16 = 1  /* bfloat16 K/V/q/out; arithmetic in float32 */
+} pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,       /* null pointer, negative or inconsistent size */
+  PKV_EUNSUPPORTED = -2, /* head_dim / head grouping / dtype combination not built */
+  PKV_EALIGN = -3,       /* a tensor pointer is not 16-byte aligned */
+  PKV_ECUDA = -4,        /* the CUDA runtime reported an error (query or launch) */
+  PKV_EWORKSPACE = -5    /* split workspace missing or smaller than required */
+} pkv_status;
+
+/* Device error word bits (pkv_get_device_error). */
+#define PKV_DERR_SLOT_RANGE 0x1u     /* kv_store: slot >= num_blocks * block_size or < -1 */
+#define PKV_DERR_BLOCK_RANGE 0x2u    /* a block table entry that must be read is outside [0, num_blocks) */
+#define PKV_DERR_LEN_RANGE 0x4u      /* context_lens / cu_seqlens inconsistent with the table width or the batch */
+#define PKV_DERR_WAIT_TIMEOUT 0x8u   /* a pipeline wait gave up (about 1 s); the results are invalid */
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pkv_version(void);
+
+/* Static string for a pkv_status value. */
+const char* pkv_status_string(int status);
+
+/*
+ * Reads (and with reset != 0 clears) the current device's error word.
+ * Synchronises the device.  Returns PKV_OK or PKV_ECUDA.
+ */
+int pkv_get_device_error(uint32_t* flags, int reset);
+
+/*
+ * kv_store: for every i in [0, num_tokens) with slot_mapping[i] >= 0,
+ *   k_cache[slot / block_size, slot % block_size, :, :] = k[i, :, :]   and the same for v.
+ * slot_mapping[i] == -1 (batch padding) writes nothing.  A byte copy: the
+ * result is bit-exact, and cache bytes of other slots are untouched.
+ *
+ *   k, v            device, [num_tokens, num_kv_heads, head_dim], contiguous
+ *   k_cache, v_cache device, [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping    device, int32 [num_tokens]
+ *   num_tokens >= 0 (0 launches nothing); num_kv_heads * head_dim * element size
+ *   must be a multiple of 16 bytes.
+ * Duplicate slots among rows are a caller error (which row lands is unspecified).
+ */
+int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                 const int32_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype,
+                 pkv_stream_t stream);
+
+/*
+ * Bytes of split workspace pkv_paged_decode_attn needs on the current device
+ * for these sizes (0 when num_splits == 1).  num_splits: 0 = automatic
+ * (the context tokens of the whole batch are divided evenly over a grid sized
+ * to the GPU), S >= 1 = every sequence's context cut into S equal parts.
+ * Returns 0 and sets nothing on invalid sizes; a CUDA query failure also returns 0.
+ */
+size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                                        int32_t num_splits);
+
+/*
+ * paged_decode_attn: for each sequence b and query head h (kv head g = h / G,
+ * G = num_q_heads / num_kv_heads), with T = context_lens[b]:
+ *   s_t = scale * q[b, h, :] . K_t,    K_t = k_cache[block_tables[b, t / block_size], t % block_size, g, :]
+ *   out[b, h, :] = sum_{t < T} softmax(s)_t V_t       (V_t likewise from v_cache)
+ * T == 0 (padding row) reads nothing and writes zeros.  Only the first
+ * ceil(T / block_size) entries of row b of block_tables are read; -1 padding
+ * or stale ids to their right are never touched.
+ *
+ *   out             device, [batch, num_q_heads, head_dim]
+ *   q               device, [batch, num_q_heads, head_dim]
+ *   k_cache,v_cache device, [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables    device, int32 [batch, max_blocks_per_seq]
+ *   context_lens    device, int32 [batch], each in [0, max_blocks_per_seq * block_size]
+ *   num_splits      0 = automatic, S >= 1 = S equal parts per sequence (1 = no split)
+ *   workspace       device, >= pkv_paged_decode_workspace_bytes(...) bytes, 256-byte
+ *                   aligned; may be NULL when that is 0.  It must be zero-filled once
+ *                   after allocation; every call leaves it ready for the next one.
+ *                   Calls sharing a workspace must not overlap in time.
+ * Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; num_kv_heads in [1, 8];
+ * dtype F32 or BF16.
+ */
+int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float scale, int32_t num_splits, void* workspace,
+                          size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * paged_varlen_prefill_attn: sequence i owns query rows cu_seqlens_q[i] ..
+ * cu_seqlens_q[i+1]-1 (nq rows, the tokens computed this round) and nk =
+ * cu_seqlens_k[i+1] - cu_seqlens_k[i] keys; the first c = nk - nq keys are
+ * history.  Query row r is at absolute position c + r and, when causal, attends
+ * keys 0 .. c + r (bottom-right aligned); otherwise all nk keys.
+ *
+ * Keys/values come from the paged cache through block_tables when
+ * block_tables != NULL (the new rows must have been stored first with
+ * pkv_kv_store), else from the packed k, v rows cu_seqlens_k[i] .. cu_seqlens_k[i+1]-1.
+ *
+ *   out             device, [total_q, num_q_heads, head_dim]
+ *   q               device, [total_q, num_q_heads, head_dim]
+ *   k, v            device, [total_k, num_kv_heads, head_dim]; read only when block_tables == NULL
+ *   k_cache,v_cache device, cache layout above; read only when block_tables != NULL
+ *   cu_seqlens_q/k  device, int32 [batch + 1], non-decreasing, starting at 0
+ *   max_seqlen_q    >= every nq (sizes the grid); max_seqlen_k >= every nk
+ *   block_tables    device, int32 [batch, max_blocks_per_seq] or NULL
+ *   causal          1 = causal (bottom-right), 0 = full
+ * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.
+ */
+int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const void* v,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                  int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float scale, int32_t causal, pkv_dtype dtype,
+                                  pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -123,8 +123,11 @@ def prepare_decode(seqs: list[dict], block_size: int) -> dict:
         table = seq["block_table"]
         if len(table) != blocks_needed(length, block_size):
             raise ValueError("decode expects exactly blocks_needed(length) blocks in the table")
-        last_block_num_tokens = length - (len(table) - 1) * block_size
-        slot_mapping.append(table[-1] * block_size + last_block_num_tokens - 1)
+        if length == 0:
+            slot_mapping.append(-1)  # padding row (section 5): nothing stored, nothing read
+        else:
+            last_block_num_tokens = length - (len(table) - 1) * block_size
+            slot_mapping.append(table[-1] * block_size + last_block_num_tokens - 1)
         positions.append(length - 1)
         context_lens.append(length)
     return {

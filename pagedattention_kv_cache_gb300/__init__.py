@@ -1,0 +1,19 @@
+"""Paged KV-cache attention for GB300 (sm_103a).
+
+``ops`` binds libpagedkv.so (kv_store, paged_decode_attn,
+paged_varlen_prefill_attn); ``metadata`` builds the host-side int32 arrays
+they consume; ``workloads`` draws seeded synthetic inputs.
+"""
+
+from . import metadata, ops, workloads  # noqa: F401
+from .ops import (  # noqa: F401
+    decode_workspace,
+    decode_workspace_bytes,
+    device_error,
+    kv_store,
+    paged_decode_attn,
+    paged_varlen_prefill_attn,
+)
+
+__all__ = ["kv_store", "paged_decode_attn", "paged_varlen_prefill_attn", "decode_workspace",
+           "decode_workspace_bytes", "device_error", "metadata", "ops", "workloads"]

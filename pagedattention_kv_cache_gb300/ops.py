@@ -1,0 +1,159 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Each function takes torch tensors that already live on the current CUDA
+device, checks dtype / shape / contiguity, and passes raw pointers and sizes
+to libpagedkv.so on the current torch stream.  Every step of the path runs
+in the library's CUDA kernels; nothing here computes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float32: _lib.F32, torch.bfloat16: _lib.BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16") from None
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, ndim=None, cuda=True) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+             slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write k/v rows [N, Hkv, D] into k_cache/v_cache [blocks, bs, Hkv, D] at slot_mapping (-1 skips)."""
+    for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, dtype=k.dtype)
+    _need(slot_mapping, "slot_mapping", dtype=torch.int32, ndim=1)
+    if k.dim() != 3 or v.shape != k.shape or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected k, v [N, Hkv, D] and caches [blocks, bs, Hkv, D]")
+    if k_cache.shape[2:] != k.shape[1:] or slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError("k/v rows and the cache disagree on (Hkv, D), or slot_mapping length differs")
+    nb, bs, hkv, d = k_cache.shape
+    st = _lib.load().pkv_kv_store(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                  k.shape[0], nb, bs, hkv, d, _dtype_code(k), _stream(stream))
+    _lib.check("pkv_kv_store", st)
+
+
+def decode_workspace_bytes(batch: int, num_q_heads: int, head_dim: int, num_splits: int = 0) -> int:
+    """Bytes of split workspace paged_decode_attn needs on the current device."""
+    return int(_lib.load().pkv_paged_decode_workspace_bytes(batch, num_q_heads, head_dim, num_splits))
+
+
+def decode_workspace(batch: int, num_q_heads: int, head_dim: int, num_splits: int = 0,
+                     device=None) -> torch.Tensor | None:
+    """Allocate a zero-filled workspace (uint8) for paged_decode_attn, or None when none is needed."""
+    n = decode_workspace_bytes(batch, num_q_heads, head_dim, num_splits)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *,
+                      num_splits: int = 0, workspace: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention through block tables; returns out [B, Hq, D] (same dtype as q).
+
+    num_splits: 0 = automatic split over the context, S >= 1 = S equal parts.
+    workspace: from decode_workspace(); allocated (zero-filled) when None.
+    """
+    _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", dtype=q.dtype, ndim=4)
+    _need(v_cache, "v_cache", dtype=q.dtype, ndim=4)
+    _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _need(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes between q, caches, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=q.dtype)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, d, num_splits, device=q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().pkv_paged_decode_attn(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, hq, hkv, d, bs, nb, ctypes.c_float(scale), num_splits, ws_ptr, ws_bytes,
+        _dtype_code(q), _stream(stream))
+    _lib.check("pkv_paged_decode_attn", st)
+    return out
+
+
+def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                              max_seqlen_q: int, max_seqlen_k: int, scale: float, *,
+                              k: torch.Tensor | None = None, v: torch.Tensor | None = None,
+                              k_cache: torch.Tensor | None = None, v_cache: torch.Tensor | None = None,
+                              block_tables: torch.Tensor | None = None, causal: bool = True,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Packed varlen prefill attention; keys through block_tables (cache) or from packed k/v."""
+    _need(q, "q", ndim=3)
+    _need(cu_seqlens_q, "cu_seqlens_q", dtype=torch.int32, ndim=1)
+    _need(cu_seqlens_k, "cu_seqlens_k", dtype=torch.int32, ndim=1)
+    if cu_seqlens_k.shape != cu_seqlens_q.shape:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k lengths differ")
+    B = cu_seqlens_q.shape[0] - 1
+    total_q, hq, d = q.shape
+    if block_tables is not None:
+        _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+        _need(k_cache, "k_cache", dtype=q.dtype, ndim=4)
+        _need(v_cache, "v_cache", dtype=q.dtype, ndim=4)
+        nb, bs, hkv, _ = k_cache.shape
+        mb = block_tables.shape[1]
+        if block_tables.shape[0] != B:
+            raise ValueError("block_tables rows must equal the batch")
+    else:
+        if k is None or v is None:
+            raise ValueError("without block_tables the packed k and v are required")
+        _need(k, "k", dtype=q.dtype, ndim=3)
+        _need(v, "v", dtype=q.dtype, ndim=3)
+        hkv = k.shape[1]
+        nb = bs = mb = 0
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=q.dtype)
+    st = _lib.load().pkv_paged_varlen_prefill_attn(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables), mb, B, hq, hkv, d,
+        bs, nb, ctypes.c_float(scale), 1 if causal else 0, _dtype_code(q), _stream(stream))
+    _lib.check("pkv_paged_varlen_prefill_attn", st)
+    return out
+
+
+def device_error(reset: bool = True) -> int:
+    """Read (and by default clear) the current device's error word; synchronises the device."""
+    flags = ctypes.c_uint32(0)
+    _lib.check("pkv_get_device_error", _lib.load().pkv_get_device_error(ctypes.byref(flags), 1 if reset else 0))
+    return int(flags.value)

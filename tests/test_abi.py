@@ -1,0 +1,153 @@
+"""The C ABI: the library loads and exports every declared symbol (CPU), and
+argument errors come back as status codes without launching (GPU)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kv_cache_gb300 as pkv
+from pagedattention_kv_cache_gb300 import _lib
+from pagedattention_kv_cache_gb300 import metadata as md
+from oracle import metadata as om
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def _built():
+    if not os.path.exists(_lib.LIB_PATH):
+        pytest.skip("libpagedkv.so not built (run __graft_entry__.build())")
+
+
+def test_library_exports_every_declared_symbol():
+    _built()
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    names = _declared()
+    assert {"pkv_kv_store", "pkv_paged_decode_attn", "pkv_paged_varlen_prefill_attn"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in pagedkv.h but not exported"
+    assert {n for n, _, _ in _lib.SIGNATURES} == set(names)
+
+
+def test_version_and_status_strings():
+    _built()
+    lib = _lib.load()
+    assert lib.pkv_version() >= 10000
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(_lib.EWORKSPACE) == b"workspace missing or too small"
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(_lib.LibraryMissing):
+        _lib.load()
+
+
+def test_host_metadata_matches_oracle():
+    rng = np.random.default_rng(0)
+    for bs in (1, 4, 16, 256):
+        lens = rng.integers(1, 700, size=9).tolist()
+        cached = [bs * int(rng.integers(0, n // (2 * bs) + 1)) for n in lens]
+        new = [n - c for n, c in zip(lens, cached)]
+        tables = [rng.permutation(5000)[: -(-n // bs)].tolist() for n in lens]
+        got = md.prefill_metadata(tables, cached, new, bs)
+        want = om.prepare_prefill([dict(block_table=t, num_cached_tokens=c, num_scheduled_tokens=n)
+                                   for t, c, n in zip(tables, cached, new)], bs)
+        for key in ("slot_mapping", "cu_seqlens_q", "cu_seqlens_k"):
+            assert np.array_equal(got[key], want[key]), key
+        assert got["max_seqlen_q"] == want["max_seqlen_q"] and got["max_seqlen_k"] == want["max_seqlen_k"]
+        assert (got["block_tables"] is None) == (want["block_tables"] is None)
+        dgot = md.decode_metadata(tables, lens, bs)
+        dwant = om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(tables, lens)], bs)
+        for key in ("slot_mapping", "context_lens", "block_tables"):
+            assert np.array_equal(dgot[key], dwant[key]), key
+
+
+def test_pad_decode_rows():
+    m = md.pad_decode(md.decode_metadata([[3, 1]], [6], 4), 4)
+    assert m["slot_mapping"].tolist() == [5, -1, -1, -1]
+    assert m["context_lens"].tolist() == [6, 0, 0, 0]
+    assert m["block_tables"][1:].tolist() == [[-1, -1]] * 3
+
+
+# ---------------------------------------------------------------- GPU: argument validation
+
+@pytest.mark.gpu
+def test_argument_errors_return_status():
+    lib = _lib.load()
+    dev = "cuda"
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(2, 3, dtype=torch.int32, device=dev)
+    cl = torch.ones(2, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    s = torch.cuda.current_stream().cuda_stream
+
+    def dec(**kw):
+        a = dict(out=out.data_ptr(), q=q.data_ptr(), k=kc.data_ptr(), v=kc.data_ptr(), bt=bt.data_ptr(), mb=3,
+                 cl=cl.data_ptr(), B=2, hq=4, hkv=2, d=128, bs=16, nb=4, scale=ctypes.c_float(0.1), splits=1,
+                 ws=None, wsb=0, dt=_lib.BF16)
+        a.update(kw)
+        return lib.pkv_paged_decode_attn(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["cl"], a["B"],
+                                         a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["splits"],
+                                         a["ws"], a["wsb"], a["dt"], s)
+
+    assert dec() == _lib.OK
+    assert dec(hq=3) == _lib.EINVAL
+    assert dec(d=96) == _lib.EUNSUPPORTED
+    assert dec(q=None) == _lib.EINVAL
+    assert dec(q=q.data_ptr() + 2) == _lib.EALIGN
+    assert dec(splits=0) == _lib.EWORKSPACE
+    assert dec(splits=4, ws=None) == _lib.EWORKSPACE
+    assert dec(bs=0) == _lib.EINVAL
+    assert dec(dt=7) == _lib.EUNSUPPORTED
+    assert dec(B=0) == _lib.OK
+    assert lib.pkv_paged_decode_workspace_bytes(2, 4, 128, 1) == 0
+    assert lib.pkv_paged_decode_workspace_bytes(2, 4, 128, 3) > 0
+    with pytest.raises(_lib.PagedKVError):
+        pkv.paged_decode_attn(q, kc, kc, bt, cl, 0.1, num_splits=2, workspace=torch.zeros(8, dtype=torch.uint8,
+                                                                                           device=dev))
+    k = torch.zeros(3, 2, 128, dtype=torch.bfloat16, device=dev)
+    slots = torch.zeros(3, dtype=torch.int32, device=dev)
+    st = lib.pkv_kv_store(k.data_ptr(), k.data_ptr(), kc.data_ptr(), kc.data_ptr(), slots.data_ptr(), -1, 4, 16, 2,
+                          128, _lib.BF16, s)
+    assert st == _lib.EINVAL
+    st = lib.pkv_kv_store(k.data_ptr() + 4, k.data_ptr(), kc.data_ptr(), kc.data_ptr(), slots.data_ptr(), 3, 4, 16,
+                          2, 128, _lib.BF16, s)
+    assert st == _lib.EALIGN
+    st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
+                                           bt.data_ptr(), 1, 1, None, 0, 1, 4, 2, 64, 16, 4, ctypes.c_float(0.1), 1,
+                                           _lib.BF16, s)
+    assert st == _lib.EUNSUPPORTED
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+
+
+@pytest.mark.gpu
+def test_out_of_range_indices_raise_device_error_bits():
+    # the kernels' own bounds checks turn these into error bits, never an access
+    dev = "cuda"
+    pkv.device_error(reset=True)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.float32, device=dev)
+    k = torch.ones(2, 2, 64, device=dev)
+    pkv.kv_store(k, k, kc, kc, torch.tensor([64, -5], dtype=torch.int32, device=dev))
+    assert pkv.device_error() == _lib.DERR_SLOT_RANGE
+    assert torch.count_nonzero(kc) == 0
+    q = torch.ones(1, 2, 64, device=dev)
+    bt = torch.tensor([[7]], dtype=torch.int32, device=dev)  # block 7 of a 4-block pool
+    pkv.paged_decode_attn(q, kc, kc, bt, torch.tensor([5], dtype=torch.int32, device=dev), 0.1, num_splits=1)
+    assert pkv.device_error() & _lib.DERR_BLOCK_RANGE
+    pkv.paged_decode_attn(q, kc, kc, bt, torch.tensor([17], dtype=torch.int32, device=dev), 0.1, num_splits=1)
+    assert pkv.device_error() & _lib.DERR_LEN_RANGE
+    assert pkv.device_error() == 0

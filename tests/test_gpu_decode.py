@@ -1,0 +1,141 @@
+"""GPU parity of kv_store + paged_decode_attn against the oracle (through the C-ABI)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kv_cache_gb300 as pkv
+from pagedattention_kv_cache_gb300 import metadata as md
+from pagedattention_kv_cache_gb300 import workloads as wl
+from oracle import attention as oa
+
+from _harness import as_np, assert_close, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_decode_fp32():
+    r = run_decode(wl.tiny_decode())
+    assert r["stats"]["max_abs"] < 1e-5
+
+
+def test_tiny_decode_fp32_poisoned():
+    run_decode(wl.tiny_decode(), poison=True)
+
+
+def test_qwen3_decode_b32_bf16():
+    run_decode(wl.qwen3_decode_b32())
+
+
+def test_qwen3_decode_b32_poisoned():
+    run_decode(wl.qwen3_decode_b32(), poison=True)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+def test_split_invariance_fp32(splits):
+    w = wl.random_decode(11, batch=6, max_ctx=300, min_ctx=1, block_size=16, num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, dtype=torch.float32)
+    r = run_decode(w, num_splits=splits)
+    base = run_decode(w, num_splits=1)
+    np.testing.assert_allclose(r["out"].cpu().numpy(), base["out"].cpu().numpy(), rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("block_size", [1, 2, 4, 16])
+@pytest.mark.parametrize("group", [1, 2, 4])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_brute_force_grid(block_size, group, d, dtype):
+    # every context length 1..20 in one batch
+    rng = np.random.default_rng(block_size * 1000 + group * 100 + d)
+    lens = list(range(1, 21))
+    nb = sum(math.ceil(n / block_size) for n in lens) + 3
+    perm = rng.permutation(nb).tolist()
+    tables, pos = [], 0
+    for n in lens:
+        k = math.ceil(n / block_size)
+        tables.append(perm[pos:pos + k])
+        pos += k
+    w = wl.DecodeWorkload("grid", 77, 2 * group, 2, d, block_size, nb, dtype, lens, tables)
+    for splits in (0, 1, 3):
+        run_decode(w, num_splits=splits)
+
+
+@pytest.mark.parametrize("kv_heads", [1, 2, 4, 8])
+def test_kv_head_counts(kv_heads):
+    w = wl.random_decode(5, batch=9, max_ctx=700, min_ctx=1, block_size=32, num_q_heads=2 * kv_heads,
+                         num_kv_heads=kv_heads, head_dim=128, dtype=torch.bfloat16)
+    run_decode(w)
+
+
+def test_group_8():
+    w = wl.random_decode(6, batch=5, max_ctx=400, min_ctx=1, block_size=16, num_q_heads=16, num_kv_heads=2,
+                         head_dim=128, dtype=torch.bfloat16)
+    run_decode(w)
+
+
+def test_long_context_split_decode_full_size():
+    r = run_decode(wl.long_context_decode(), gen_device="cuda", check_store=True)
+    assert r["stats"]["mean_abs"] < 1e-3
+
+
+def test_zero_context_rows_and_padding():
+    # graph-replay padding: rows with slot -1 and context length 0 read and write nothing
+    w = wl.random_decode(8, batch=5, max_ctx=90, min_ctx=1, block_size=8, num_q_heads=4, num_kv_heads=2,
+                         head_dim=64, dtype=torch.float32)
+    t = wl.decode_tensors(w, "cpu")
+    meta = md.pad_decode(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), 8)
+    dev = "cuda"
+    q = torch.randn(8, 4, 64, generator=torch.Generator().manual_seed(3)).to(dev)
+    q[:5] = t["q"].to(dev)
+    kn = torch.zeros(8, 2, 64, device=dev)
+    vn = torch.zeros(8, 2, 64, device=dev)
+    kn[:5] = t["k_new"].to(dev)
+    vn[:5] = t["v_new"].to(dev)
+    kc, vc = t["k_cache"].to(dev), t["v_cache"].to(dev)
+    gm = md.to_device(meta, dev)
+    gm["block_tables"][5:, :] = 10 ** 6  # stale ids on padded rows: never read
+    pkv.kv_store(kn, vn, kc, vc, gm["slot_mapping"])
+    out = torch.full((8, 4, 64), float("nan"), device=dev)
+    for splits in (0, 1, 4):
+        pkv.paged_decode_attn(q, kc, vc, gm["block_tables"], gm["context_lens"], w.scale, num_splits=splits, out=out)
+        torch.cuda.synchronize()
+        assert pkv.device_error() == 0
+        assert torch.all(out[5:] == 0)
+        kco, vco = oa.kv_store(as_np(t["k_cache"]), as_np(t["v_cache"]), as_np(t["k_new"]), as_np(t["v_new"]),
+                               meta["slot_mapping"][:5])
+        ref = oa.paged_decode_attention(as_np(t["q"]), kco, vco, meta["block_tables"][:5], meta["context_lens"][:5],
+                                        w.scale)
+        assert_close(out[:5], ref, torch.float32, "padded")
+    assert torch.equal(kc.cpu(), torch.from_numpy(kco)) and torch.equal(vc.cpu(), torch.from_numpy(vco))
+
+
+def test_block_permutation_bit_identical():
+    w = wl.qwen3_decode_b32()
+    r = run_decode(w)
+    g = r["tensors"]
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(9))
+    kc2 = torch.empty_like(g["k_cache"])
+    vc2 = torch.empty_like(g["v_cache"])
+    kc2[perm.cuda()] = g["k_cache"]
+    vc2[perm.cuda()] = g["v_cache"]
+    bt = r["meta"]["block_tables"]
+    bt2 = torch.where(bt >= 0, perm.cuda()[bt.clamp(min=0).long()].int(), bt)
+    out2 = pkv.paged_decode_attn(g["q"], kc2, vc2, bt2, r["meta"]["context_lens"], w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, r["out"])
+
+
+def test_repeated_calls_reuse_workspace():
+    w = wl.qwen3_decode_b32()
+    r = run_decode(w)
+    g = r["tensors"]
+    ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0)
+    outs = [pkv.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], r["meta"]["block_tables"],
+                                  r["meta"]["context_lens"], w.scale, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, r["out"])
+    # the workspace's ticket counters are back at zero
+    assert torch.count_nonzero(ws[: 4 * w.batch]) == 0

@@ -1,0 +1,96 @@
+"""GPU parity of kv_store + paged_varlen_prefill_attn against the oracle (through the C-ABI)."""
+
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kv_cache_gb300 as pkv
+from pagedattention_kv_cache_gb300 import metadata as md
+from pagedattention_kv_cache_gb300 import workloads as wl
+
+from _harness import assert_close, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def test_qwen3_prefill_prefix_chunk():
+    run_prefill(wl.qwen3_prefill_prefix())
+
+
+def test_qwen3_prefill_prefix_chunk_poisoned():
+    run_prefill(wl.qwen3_prefill_prefix(), poison=True)
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("block_size", [16, 256])
+def test_prefill_groups_and_block_sizes(group, block_size):
+    w = wl.random_prefill(group * 10 + block_size, batch=5, max_new=150, min_new=1, max_cached_blocks=3,
+                          block_size=block_size, num_q_heads=2 * group, num_kv_heads=2, head_dim=128)
+    run_prefill(w)
+
+
+def test_prefill_edge_lengths():
+    # empty sequences, single-row sequences, tile-boundary lengths
+    news = [0, 1, 63, 64, 65, 128, 129, 31, 33]
+    cached = [0, 16, 0, 32, 16, 0, 64, 48, 0]
+    tables, pos = [], 0
+    perm = np.random.default_rng(4).permutation(200).tolist()
+    for n, c in zip(news, cached):
+        k = -(-(n + c) // 16)
+        tables.append(perm[pos:pos + k])
+        pos += k
+    w = wl.PrefillWorkload("edges", 5, 4, 2, 128, 16, 200, torch.bfloat16, cached, news, tables)
+    run_prefill(w)
+
+
+def test_prefill_no_history_packed_path():
+    w = wl.random_prefill(21, batch=6, max_new=200, min_new=1, max_cached_blocks=0, block_size=16,
+                          num_q_heads=16, num_kv_heads=8, head_dim=128)
+    assert sum(w.num_cached) == 0
+    r_packed = run_prefill(w, use_tables=False)
+    r_paged = run_prefill(w, use_tables=True)
+    assert torch.equal(r_packed["out"], r_paged["out"])
+
+
+def test_prefill_non_causal():
+    w = wl.random_prefill(22, batch=4, max_new=90, min_new=1, max_cached_blocks=2, block_size=16,
+                          num_q_heads=8, num_kv_heads=4, head_dim=128)
+    run_prefill(w, causal=False)
+
+
+def test_prefix_hit_equals_full_recompute():
+    # same tokens: a prefill with a prefix-cache hit gives the last rows of a full recompute
+    bs, hq, hkv, d = 16, 8, 4, 128
+    n, c = 300, 96
+    gen = torch.Generator().manual_seed(12)
+    table = torch.randperm(40, generator=gen)[: -(-n // bs)].tolist()
+    kc = torch.randn(40, bs, hkv, d, generator=gen).to(torch.bfloat16).cuda()
+    vc = torch.randn(40, bs, hkv, d, generator=gen).to(torch.bfloat16).cuda()
+    q = torch.randn(n, hq, d, generator=gen).to(torch.bfloat16).cuda()
+    full_md = md.to_device(md.prefill_metadata([table], [0], [n], bs, always_tables=True), "cuda")
+    hit_md = md.to_device(md.prefill_metadata([table], [c], [n - c], bs, always_tables=True), "cuda")
+    scale = d ** -0.5
+    full = pkv.paged_varlen_prefill_attn(q, full_md["cu_seqlens_q"], full_md["cu_seqlens_k"], n, n, scale,
+                                         k_cache=kc, v_cache=vc, block_tables=full_md["block_tables"])
+    hit = pkv.paged_varlen_prefill_attn(q[c:].contiguous(), hit_md["cu_seqlens_q"], hit_md["cu_seqlens_k"], n - c, n,
+                                        scale, k_cache=kc, v_cache=vc, block_tables=hit_md["block_tables"])
+    torch.cuda.synchronize()
+    diff = (hit.float() - full[c:].float()).abs().max().item()
+    assert diff <= 1e-2
+
+
+def test_decode_equals_prefill_single_row():
+    w = wl.random_decode(31, batch=7, max_ctx=500, min_ctx=1, block_size=16, num_q_heads=8, num_kv_heads=4,
+                         head_dim=128, dtype=torch.bfloat16)
+    t = wl.decode_tensors(w, "cpu")
+    g = {k: v.cuda() for k, v in t.items()}
+    dm = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), "cuda")
+    dec = pkv.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], dm["block_tables"], dm["context_lens"], w.scale)
+    pm = md.prefill_metadata(w.block_tables, [n - 1 for n in w.context_lens], [1] * w.batch, w.block_size,
+                             always_tables=True)
+    gp = md.to_device(pm, "cuda")
+    pre = pkv.paged_varlen_prefill_attn(g["q"], gp["cu_seqlens_q"], gp["cu_seqlens_k"], 1, pm["max_seqlen_k"],
+                                        w.scale, k_cache=g["k_cache"], v_cache=g["v_cache"],
+                                        block_tables=gp["block_tables"])
+    torch.cuda.synchronize()
+    assert (dec.float() - pre.float()).abs().max().item() <= 1e-2
