@@ -270,10 +270,12 @@ def bench_decode(args, device, world):
     sampler = ClockSampler(device.index or 0)
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_steps")
     start.record()
     for k in range(args.steps):
         st.step(events=ev[k])
     stop.record()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
