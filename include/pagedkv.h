@@ -33,7 +33,9 @@
  *  - Pointers marked "device" must be device memory (or managed memory)
  *    of the current CUDA device; the library dereferences them only on the
  *    GPU.  Tensor pointers must be 16-byte aligned.
- *  - The caller owns every buffer.  The library allocates no device memory.
+ *  - The caller owns every buffer.  The library allocates no device memory
+ *    (pkv_paged_decode_attn_noalloc's fixed scratch is part of the library's
+ *    device image, not an allocation).
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *    nothing synchronises.  Argument errors are detected on the host and
  *    returned as a negative pkv_status before anything is launched.
@@ -67,8 +69,12 @@ typedef enum {
   PKV_EUNSUPPORTED = -2, /* head_dim / head grouping / dtype combination not built */
   PKV_EALIGN = -3,       /* a tensor pointer is not 16-byte aligned */
   PKV_ECUDA = -4,        /* the CUDA runtime reported an error (query or launch) */
-  PKV_EWORKSPACE = -5    /* split workspace missing or smaller than required */
+  PKV_EWORKSPACE = -5,   /* split workspace missing or smaller than required */
+  PKV_ESCRATCH = -6      /* pkv_paged_decode_attn_noalloc: sizes exceed its fixed scratch */
 } pkv_status;
+
+/* Size of the fixed scratch array behind pkv_paged_decode_attn_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 /* Device error word bits (pkv_get_device_error). */
 #define PKV_DERR_SLOT_RANGE 0x1u     /* kv_store: slot >= num_blocks * block_size or < -1 */
@@ -144,6 +150,40 @@ int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const v
                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                           int32_t num_blocks, float scale, int32_t num_splits, void* workspace,
                           size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * paged_decode_attn without a caller-provided workspace (no counterpart in the
+ * pages: it is an addition of this library).
+ *
+ * For callers that cannot allocate device memory -- hooks running inside
+ * another engine's execution step where the allocator is off limits,
+ * runtimes whose device memory belongs to a pool this library cannot reach,
+ * and latency-critical code that must not pay cudaMalloc's implicit
+ * synchronisation.  It computes exactly what pkv_paged_decode_attn computes,
+ * with the same arguments minus the workspace, and allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *
+ * The split workspace is a fixed array of PKV_NOALLOC_SCRATCH_BYTES bytes
+ * (8 MiB) inside the library's device image, held by every GPU that
+ * loads the library until the process exits.  Sizes whose workspace
+ * (pkv_paged_decode_workspace_bytes) exceeds it return PKV_ESCRATCH without
+ * launching; with 152 SMs, 16 query heads and head_dim 128 the automatic
+ * split fits batches up to about 700.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call clears the array's ticket counters
+ * (cudaMemsetAsync on `stream`) and then reuses the array, which keeps the
+ * previous call's contents otherwise.  All calls on a device share the one
+ * array: calls that overlap on the GPU (different streams without ordering)
+ * race and give wrong results.
+ */
+int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks, float scale, int32_t num_splits, pkv_dtype dtype,
+                                  pkv_stream_t stream);
 
 /*
  * paged_varlen_prefill_attn: sequence i owns query rows cu_seqlens_q[i] ..

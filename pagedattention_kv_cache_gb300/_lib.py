@@ -22,6 +22,9 @@ EUNSUPPORTED = -2
 EALIGN = -3
 ECUDA = -4
 EWORKSPACE = -5
+ESCRATCH = -6
+
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 # device error word bits
 DERR_SLOT_RANGE = 0x1
@@ -42,6 +45,8 @@ SIGNATURES = [
     ("pkv_paged_decode_workspace_bytes", _S, [_I, _I, _I, _I]),
     ("pkv_paged_decode_attn", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, ctypes.c_int, _P]),
+    ("pkv_paged_decode_attn_noalloc", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int, _P]),
     ("pkv_paged_varlen_prefill_attn", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int, _P]),
 ]

@@ -68,6 +68,7 @@ extern "C" const char* pkv_status_string(int status) {
     case PKV_EALIGN: return "pointer not 16-byte aligned";
     case PKV_ECUDA: return "CUDA runtime error";
     case PKV_EWORKSPACE: return "workspace missing or too small";
+    case PKV_ESCRATCH: return "sizes need more split scratch than the no-allocation entry point holds";
     default: return "unknown status";
   }
 }

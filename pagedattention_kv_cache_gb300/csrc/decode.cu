@@ -26,6 +26,7 @@
 //    each part writes (o, m, l) to the workspace and the last CTA to finish
 //    a sequence (atomic ticket, no waiting) merges the parts by log-sum-exp.
 #include <cfloat>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -681,4 +682,66 @@ extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cac
   }
   if (head_dim == 128) return dispatch_g<float, 128>(p, group, info.sms, stream);
   return dispatch_g<float, 64>(p, group, info.sms, stream);
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+//
+// Some callers cannot allocate device memory for the split workspace: code
+// running inside another engine's execution hook that must not touch the
+// allocator, runtimes whose memory is owned by a pool this library cannot
+// see, and latency-critical paths that must avoid cudaMalloc's implicit
+// device synchronisation.  pkv_paged_decode_attn_noalloc serves them with a
+// fixed-size scratch array that lives in the library's own device image.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;  // 8 MiB per device
+
+// Device-side scratch.  In host code this name is only a host stand-in; its
+// device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of this device's scratch array, looked up once per device
+// with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return PKV_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PKV_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                             int32_t num_blocks, float scale, int32_t num_splits, pkv_dtype dtype,
+                                             pkv_stream_t stream) {
+  if (batch < 0 || num_q_heads <= 0 || head_dim <= 0 || num_splits < 0) return PKV_EINVAL;
+  pkv::DeviceInfo info;
+  if (pkv::device_info(&info) != PKV_OK) return PKV_ECUDA;
+  size_t off_o = 0, off_ml = 0;
+  const size_t need = workspace_layout(batch, num_q_heads, head_dim, num_splits, info.sms, &off_o, &off_ml);
+  if (need > kNoAllocScratchBytes) return PKV_ESCRATCH;
+  void* scratch = nullptr;
+  if (need > 0) {
+    const int st = noalloc_scratch(&scratch);
+    if (st != PKV_OK) return st;
+    // the ticket counters must start at zero; the array keeps the previous call's contents
+    if (cudaMemsetAsync(scratch, 0, off_o, stream) != cudaSuccess) return PKV_ECUDA;
+  }
+  return pkv_paged_decode_attn(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                               num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, num_splits, scratch,
+                               need > 0 ? kNoAllocScratchBytes : 0, dtype, stream);
 }

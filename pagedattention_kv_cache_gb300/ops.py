@@ -112,6 +112,29 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     return out
 
 
+def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *,
+                              num_splits: int = 0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_decode_attn for callers that cannot allocate: the split workspace is the
+    library's fixed 8 MiB device array (calls on one device must not overlap)."""
+    _need(q, "q", ndim=3)
+    _need(k_cache, "k_cache", dtype=q.dtype, ndim=4)
+    _need(v_cache, "v_cache", dtype=q.dtype, ndim=4)
+    _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _need(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    B, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=q.dtype)
+    st = _lib.load().pkv_paged_decode_attn_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, hq, hkv, d, bs, nb, ctypes.c_float(scale), num_splits, _dtype_code(q),
+        _stream(stream))
+    _lib.check("pkv_paged_decode_attn_noalloc", st)
+    return out
+
+
 def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                               max_seqlen_q: int, max_seqlen_k: int, scale: float, *,
                               k: torch.Tensor | None = None, v: torch.Tensor | None = None,
