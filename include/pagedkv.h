@@ -200,21 +200,27 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *   q               device, [total_q, num_q_heads, head_dim]
  *   k, v            device, [total_k, num_kv_heads, head_dim]; read only when block_tables == NULL
  *   k_cache,v_cache device, cache layout above; read only when block_tables != NULL
- *   cu_seqlens_q/k  device, int32 [batch + 1], non-decreasing, starting at 0
+ *   cu_seqlens_q/k  device, int32 [batch + 1], non-decreasing, starting at 0; every
+ *                   nk >= nq, cu_seqlens_q[batch] <= total_q and, without block_tables,
+ *                   cu_seqlens_k[batch] <= total_k (a sequence breaking these is skipped
+ *                   and raises PKV_DERR_LEN_RANGE)
  *   max_seqlen_q    >= every nq (sizes the grid); max_seqlen_k >= every nk
  *   block_tables    device, int32 [batch, max_blocks_per_seq] or NULL
+ *   total_q, total_k rows of q/out and of the packed k/v (total_k is ignored with block_tables)
  *   causal          1 = causal (bottom-right), 0 = full
- * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.
+ * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.  Block sizes that are a
+ * multiple of 128, or a divisor of 128 of at least 8, and the packed path run on
+ * the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel.
  */
 int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const void* v,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                                   int32_t max_seqlen_q, int32_t max_seqlen_k,
                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                  int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                  int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                                  float scale, int32_t causal, pkv_dtype dtype,
-                                  pkv_stream_t stream);
+                                  int32_t batch, int32_t total_q, int32_t total_k,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_blocks, float scale,
+                                  int32_t causal, pkv_dtype dtype, pkv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -48,7 +48,8 @@ SIGNATURES = [
     ("pkv_paged_decode_attn_noalloc", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int, _P]),
     ("pkv_paged_varlen_prefill_attn", ctypes.c_int,
-     [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int, _P]),
+     [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int,
+      _P]),
 ]
 
 _lib = None

@@ -21,6 +21,12 @@ struct DeviceInfo {
 int device_info(DeviceInfo* info);            // returns PKV_OK or PKV_ECUDA
 unsigned int* device_error_word(int* status);  // device address of this device's error word
 
+// Encodes a 3-D bf16 tensor map (dims innermost first, rows of d0 contiguous
+// elements) with 128-byte swizzle for tiled TMA loads of box b0 x b1 x b2.
+// `map` points to a CUtensorMap (64-byte aligned, 128 bytes).
+int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+                   uint32_t b2);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- device side

@@ -16,7 +16,7 @@
 // them.  Q K^T and P V run on tensor cores (mma.sync m16n8k16, bf16 in,
 // fp32 accumulate) with an online softmax in registers; K/V tiles are
 // double-buffered in XOR-swizzled shared memory with cp.async.
-#include "common.cuh"
+#include "prefill_args.cuh"
 
 namespace {
 
@@ -39,6 +39,8 @@ struct Params {
   const int32_t* cu_k;
   const int32_t* block_tables;
   unsigned int* err;
+  int total_q;
+  int total_k;
   int max_blocks;
   int batch;
   int hq;
@@ -138,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
   const int nk = __ldg(p.cu_k + seq + 1) - k_begin;
   const int tok0 = blockIdx.x * TQ;
   if (tok0 >= nq) return;
-  if (nk < nq || (p.block_tables && nk > p.max_blocks * p.block_size)) {
+  if (nk < nq || q_begin + nq > p.total_q || (p.block_tables && nk > p.max_blocks * p.block_size) ||
+      (!p.block_tables && k_begin + nk > p.total_k)) {
     if (threadIdx.x == 0) pkv::raise_error(p.err, PKV_DERR_LEN_RANGE);
     return;
   }
@@ -334,32 +337,59 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
                                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                                              int32_t max_seqlen_q, int32_t max_seqlen_k,
                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                             int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                             int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                                             float scale, int32_t causal, pkv_dtype dtype,
+                                             int32_t batch, int32_t total_q, int32_t total_k, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                             int32_t num_blocks, float scale, int32_t causal, pkv_dtype dtype,
                                              pkv_stream_t stream) {
-  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seqlen_q < 0 ||
-      max_seqlen_k < 0)
+  if (batch < 0 || total_q < 0 || total_k < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_seqlen_q < 0 || max_seqlen_k < 0)
     return PKV_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
   if (dtype != PKV_BF16 || head_dim != kD) return PKV_EUNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_EUNSUPPORTED;
   if (causal != 0 && causal != 1) return PKV_EINVAL;
-  if (batch == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (batch == 0 || max_seqlen_q == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !cu_seqlens_q || !cu_seqlens_k) return PKV_EINVAL;
   if (block_tables) {
     if (!k_cache || !v_cache || block_size <= 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PKV_EINVAL;
-    if (static_cast<long long>(max_blocks_per_seq) * block_size > INT32_MAX) return PKV_EINVAL;
+    if (static_cast<long long>(max_blocks_per_seq) * block_size > INT32_MAX ||
+        static_cast<long long>(num_blocks) * block_size > INT32_MAX)
+      return PKV_EINVAL;
     if (!pkv::aligned16(k_cache) || !pkv::aligned16(v_cache)) return PKV_EALIGN;
   } else {
-    if (!k || !v) return PKV_EINVAL;
+    if (!k || !v || total_k == 0) return PKV_EINVAL;
     if (!pkv::aligned16(k) || !pkv::aligned16(v)) return PKV_EALIGN;
   }
   if (!pkv::aligned16(out) || !pkv::aligned16(q)) return PKV_EALIGN;
   int st = PKV_OK;
   unsigned int* err = pkv::device_error_word(&st);
   if (st != PKV_OK) return st;
+
+  pkv::PrefillArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.block_tables = block_tables;
+  a.err = err;
+  a.total_q = total_q;
+  a.total_k = block_tables ? 0 : total_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_blocks = max_blocks_per_seq;
+  a.batch = batch;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.causal = causal;
+  a.group = group;
+  if (pkv::prefill_tc_supported(a)) return pkv::prefill_tc_launch(a, stream);
 
   Params p{};
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -372,6 +402,8 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
   p.cu_k = cu_seqlens_k;
   p.block_tables = block_tables;
   p.err = err;
+  p.total_q = total_q;
+  p.total_k = total_k;
   p.max_blocks = max_blocks_per_seq;
   p.batch = batch;
   p.hq = num_q_heads;

@@ -1,0 +1,40 @@
+// Arguments shared by the two prefill kernels (tcgen05 and mma.sync) and the
+// C entry point that chooses between them.
+#pragma once
+
+#include "common.cuh"
+
+namespace pkv {
+
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* block_tables;  // null: keys from the packed k, v
+  unsigned int* err;
+  int total_q;  // rows of q / out
+  int total_k;  // rows of the packed k / v (0 when block_tables is used)
+  int max_seqlen_q;
+  int max_blocks;
+  int batch;
+  int hq;
+  int hkv;
+  int block_size;
+  int num_blocks;
+  float scale;
+  int causal;
+  int group;  // hq / hkv
+};
+
+// Tensor-core (tcgen05 + TMEM + TMA) path; requires head_dim 128, bf16, and
+// for the paged case a block size that is a multiple of 128 or a divisor of
+// 128 of at least 8.
+bool prefill_tc_supported(const PrefillArgs& a);
+int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,415 @@
+// paged_varlen_prefill_attn on the 5th-generation tensor cores (tcgen05).
+//
+// What is computed is the same as the mma.sync kernel in prefill.cu
+// ("3.6 ModelRunner, CUDA Graph, and benchmarks", section 2, prepare_prefill):
+// query row r of sequence i sits at absolute position c + r (c = nk - nq
+// history tokens) and, causally, attends keys 0..c + r, read through the
+// block table (or from the packed k/v rows when there is no history).
+//
+// How: a CTA owns one (query tile, sequence, KV head).  The tile's 128 rows
+// are (token, query head of the KV group) pairs, token-major, so one TMA box
+// of q [total_q, Hq, D] covers them and every K/V tile serves all G heads.
+//   warp 0     TMA producer: Q once, then K and V tiles of 128 keys into a
+//              2-stage ring (128-byte swizzled, one box per 64-wide d slab;
+//              paged tiles are gathered block piece by block piece).
+//   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (two S buffers so
+//              the next tile's S overlaps the softmax of this one), then
+//              O += P V with P read from TMEM and V as an MN-major operand.
+//   warps 2-5  softmax, one thread per TMEM lane (= query row): scale, mask,
+//              row max, exp2, bf16 P written back over its S buffer; O is
+//              rescaled in TMEM only when the row max grows by more than 2^8;
+//              final normalisation and store.
+// Every wait is bounded; on a timeout the CTA records an error, skips the
+// remaining waits and still frees its TMEM.
+#include "prefill_args.cuh"
+#include "tcgen05.cuh"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kD = 128;
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;  // S buffers at columns 0 and 128, O at 256
+constexpr uint32_t kSlabQ = kBM * 128;
+constexpr uint32_t kSlabKV = kBN * 128;
+constexpr uint32_t kTileQ = 2 * kSlabQ;
+constexpr uint32_t kTileKV = 2 * kSlabKV;
+constexpr uint32_t kBarOffset = kTileQ + 2 * kStages * kTileKV;
+constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
+constexpr float kRescaleLog2 = 8.0f;
+
+enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, P_FULL = 9, O_DONE = 11, NUM_BARS = 12 };
+
+struct TcParams {
+  __nv_bfloat16* out;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* block_tables;
+  unsigned int* err;
+  int total_q;
+  int total_k;
+  int max_blocks;
+  int hq;
+  int hkv;
+  int block_size;
+  int num_blocks;
+  float scale_log2;
+  int causal;
+  int paged;
+  int piece_rows;  // rows per K/V TMA box (paged: min(block_size, kBN))
+  int q_tiles;
+};
+
+struct Waiter {
+  volatile int* abort_flag;
+  unsigned int* err;
+  __device__ __forceinline__ void operator()(uint64_t* bar, uint32_t parity) const {
+    if (*abort_flag) return;
+    if (!mbar_wait(bar, parity)) {
+      *abort_flag = 1;
+      raise_error(err, PKV_DERR_WAIT_TIMEOUT);
+    }
+  }
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  constexpr int TQ = kBM / G;
+  const int seq = blockIdx.y;
+  const int g = blockIdx.z;
+  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
+  const int q_begin = __ldg(p.cu_q + seq);
+  const int nq = __ldg(p.cu_q + seq + 1) - q_begin;
+  const int k_begin = __ldg(p.cu_k + seq);
+  const int nk = __ldg(p.cu_k + seq + 1) - k_begin;
+  const int tok0 = qt * TQ;
+  if (tok0 >= nq) return;
+  if (nk < nq || q_begin + nq > p.total_q || (p.paged && nk > p.max_blocks * p.block_size) ||
+      (!p.paged && k_begin + nk > p.total_k)) {
+    if (threadIdx.x == 0) raise_error(p.err, PKV_DERR_LEN_RANGE);
+    return;
+  }
+  const int cached = nk - nq;
+  const int tok_last = min(nq, tok0 + TQ) - 1;
+  const int keys_needed = p.causal ? cached + tok_last + 1 : nk;
+  const int n_tiles = (keys_needed + kBN - 1) / kBN;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  unsigned char* sq = smem;
+  unsigned char* sk = smem + kTileQ;
+  unsigned char* sv = sk + kStages * kTileKV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(&bars[Q_FULL], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[K_FULL + s], 1);
+      mbar_init(&bars[V_FULL + s], 1);
+      mbar_init(&bars[KV_EMPTY + s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[S_FULL + b], 1);
+      mbar_init(&bars[P_FULL + b], 128);
+    }
+    mbar_init(&bars[O_DONE], 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter wait{abort_flag, p.err};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tensormap(&tm_q);
+      tc::prefetch_tensormap(&tm_k);
+      tc::prefetch_tensormap(&tm_v);
+      mbar_expect_tx(&bars[Q_FULL], kTileQ);
+      tc::tma_load_3d(sq, &tm_q, 0, g * G, q_begin + tok0, &bars[Q_FULL]);
+      tc::tma_load_3d(sq + kSlabQ, &tm_q, 64, g * G, q_begin + tok0, &bars[Q_FULL]);
+      mbar_arrive(&bars[Q_FULL]);
+      const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kStages;
+        const int use = j / kStages;
+        if (use > 0) wait(&bars[KV_EMPTY + st], (use - 1) & 1);
+        unsigned char* kd = sk + st * kTileKV;
+        unsigned char* vd = sv + st * kTileKV;
+        const int key0 = j * kBN;
+        if (p.paged) {
+          const uint32_t piece_bytes = p.piece_rows * 128u;
+          for (int r = 0; r < kBN; r += p.piece_rows) {
+            const int key = key0 + r;
+            if (key >= nk) break;
+            const int blk = key / p.block_size;
+            const int phys = __ldg(table + blk);
+            if (phys < 0 || phys >= p.num_blocks) {
+              raise_error(p.err, PKV_DERR_BLOCK_RANGE);
+              continue;
+            }
+            const int row = phys * p.block_size + (key - blk * p.block_size);
+            mbar_expect_tx(&bars[K_FULL + st], 2 * piece_bytes);
+            tc::tma_load_3d(kd + r * 128, &tm_k, 0, g, row, &bars[K_FULL + st]);
+            tc::tma_load_3d(kd + kSlabKV + r * 128, &tm_k, 64, g, row, &bars[K_FULL + st]);
+            mbar_expect_tx(&bars[V_FULL + st], 2 * piece_bytes);
+            tc::tma_load_3d(vd + r * 128, &tm_v, 0, g, row, &bars[V_FULL + st]);
+            tc::tma_load_3d(vd + kSlabKV + r * 128, &tm_v, 64, g, row, &bars[V_FULL + st]);
+          }
+        } else {
+          const int row = k_begin + key0;
+          mbar_expect_tx(&bars[K_FULL + st], kTileKV);
+          tc::tma_load_3d(kd, &tm_k, 0, g, row, &bars[K_FULL + st]);
+          tc::tma_load_3d(kd + kSlabKV, &tm_k, 64, g, row, &bars[K_FULL + st]);
+          mbar_expect_tx(&bars[V_FULL + st], kTileKV);
+          tc::tma_load_3d(vd, &tm_v, 0, g, row, &bars[V_FULL + st]);
+          tc::tma_load_3d(vd + kSlabKV, &tm_v, 64, g, row, &bars[V_FULL + st]);
+        }
+        mbar_arrive(&bars[K_FULL + st]);
+        mbar_arrive(&bars[V_FULL + st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
+      const uint32_t q_addr = smem_u32(sq);
+      wait(&bars[Q_FULL], 0);
+      auto issue_qk = [&](int j) {
+        const int st = j % kStages;
+        wait(&bars[K_FULL + st], (j / kStages) & 1);
+        tc::fence_after_sync();
+        const uint32_t k_addr = smem_u32(sk + st * kTileKV);
+        const uint32_t d = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSlabQ + (kk & 3) * 32;
+          const uint64_t a = tc::smem_desc(q_addr + off, 16, 1024);
+          const uint64_t b = tc::smem_desc(k_addr + (kk >> 2) * kSlabKV + (kk & 3) * 32, 16, 1024);
+          tc::mma_ss(d, a, b, idesc_qk, kk > 0);
+        }
+        tc::commit(&bars[S_FULL + (j & 1)]);
+      };
+      issue_qk(0);
+      for (int j = 0; j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) issue_qk(j + 1);
+        const int st = j % kStages;
+        wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
+        wait(&bars[V_FULL + st], (j / kStages) & 1);
+        tc::fence_after_sync();
+        const uint32_t v_addr = smem_u32(sv + st * kTileKV);
+        const uint32_t pcol = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = tc::smem_desc(v_addr + kk * 16 * 128, kSlabKV, 1024);
+          tc::mma_ts(tmem + kColO, pcol + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&bars[KV_EMPTY + st]);
+        tc::commit(&bars[O_DONE]);
+      }
+      // the epilogue waits for the last P.V; wait here too so no MMA is in flight at teardown
+      wait(&bars[O_DONE], (n_tiles - 1) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int tok = tok0 + row / G;
+    const int head = row % G;
+    const int pos = cached + tok;  // absolute position of this query row
+    const bool row_valid = tok < nq;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    uint32_t r[128];
+
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      const int key0 = j * kBN;
+      if (key0 + kBN > nk) {
+        // rows of this V tile past the last key hold whatever the block had
+        // there (or nothing was loaded): zero them so 0 * stale never reaches O
+        const int st = j % kStages;
+        wait(&bars[V_FULL + st], (j / kStages) & 1);
+        unsigned char* vt = sv + st * kTileKV;
+        const int first = nk - key0;
+        for (int idx = (warp - 2) * 32 + lane; idx < (kBN - first) * 16; idx += 128) {
+          const int rr = first + idx / 16;
+          const int ch = idx % 16;
+          *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      wait(&bars[S_FULL + b], (j >> 1) & 1);
+      tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(lane_addr + b * 128 + c * 32, r + c * 32);
+      tc::tmem_wait_ld();
+      const bool need_mask = key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float x = __uint_as_float(r[c]) * p.scale_log2;
+        if (need_mask && key0 + c > lim) x = -INFINITY;
+        r[c] = __float_as_uint(x);
+        mt = fmaxf(mt, x);
+      }
+      const float m_new = fmaxf(m_run, mt);
+      const bool grow = m_new > m_run + kRescaleLog2 || (m_run == -INFINITY && m_new != -INFINITY);
+      if (__any_sync(0xffffffffu, grow)) {
+        const float factor = (m_run == -INFINITY || m_new <= m_run) ? 1.f : exp2f(m_run - m_new);
+        if (j > 0) {
+          wait(&bars[O_DONE], (j - 1) & 1);
+          tc::fence_after_sync();
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            tc::tmem_st32(lane_addr + kColO + c * 32, o);
+          }
+          tc::tmem_wait_st();
+        }
+        l_run *= factor;
+        m_run = fmaxf(m_run, m_new);
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      // P = exp2(s - m) rounded to bf16, packed two per column over the S buffer;
+      // the row sum adds the same rounded values
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = exp2f(__uint_as_float(r[2 * c]) - m_use);
+        const float p1 = exp2f(__uint_as_float(r[2 * c + 1]) - m_use);
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        l_run += __low2float(pb) + __high2float(pb);
+        r[c] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      tc::tmem_st32(lane_addr + b * 128, r);
+      tc::tmem_st32(lane_addr + b * 128 + 32, r + 32);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars[P_FULL + b]);
+    }
+
+    wait(&bars[O_DONE], (n_tiles - 1) & 1);
+    tc::fence_after_sync();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    __nv_bfloat16* dst =
+        p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + head) * kD;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+      tc::tmem_wait_ld();
+      if (row_valid) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float f[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
+          reinterpret_cast<uint4*>(dst + c * 32 + e)[0] = Chunk<__nv_bfloat16>::pack(f);
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int G>
+int launch(const PrefillArgs& a, cudaStream_t stream) {
+  constexpr int TQ = kBM / G;
+  alignas(64) CUtensorMap tm_q, tm_k, tm_v;
+  if (encode_bf16_3d(&tm_q, a.q, kD, a.hq, a.total_q, 64, G, TQ) != PKV_OK) return PKV_ECUDA;
+  const bool paged = a.block_tables != nullptr;
+  const int piece = paged ? (a.block_size < kBN ? a.block_size : kBN) : kBN;
+  const void* kb = paged ? a.k_cache : a.k;
+  const void* vb = paged ? a.v_cache : a.v;
+  const uint64_t rows = paged ? static_cast<uint64_t>(a.num_blocks) * a.block_size : a.total_k;
+  if (encode_bf16_3d(&tm_k, kb, kD, a.hkv, rows, 64, 1, piece) != PKV_OK) return PKV_ECUDA;
+  if (encode_bf16_3d(&tm_v, vb, kD, a.hkv, rows, 64, 1, piece) != PKV_OK) return PKV_ECUDA;
+  TcParams p{};
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.block_tables = a.block_tables;
+  p.err = a.err;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.max_blocks = a.max_blocks;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.block_size = a.block_size;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.causal = a.causal;
+  p.paged = paged ? 1 : 0;
+  p.piece_rows = piece;
+  p.q_tiles = (a.max_seqlen_q + TQ - 1) / TQ;
+  auto kernel = prefill_tc_kernel<G>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
+  dim3 grid(p.q_tiles, a.batch, a.hkv);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+namespace pkv {
+
+bool prefill_tc_supported(const PrefillArgs& a) {
+  if (a.group != 1 && a.group != 2 && a.group != 4 && a.group != 8) return false;
+  if (a.total_q <= 0) return false;
+  if (a.block_tables) {
+    const int bs = a.block_size;
+    const bool whole_tiles = bs % kBN == 0;
+    const bool pieces = bs >= 8 && kBN % bs == 0;
+    if (!(whole_tiles || pieces)) return false;
+    if (static_cast<long long>(a.num_blocks) * bs <= 0) return false;
+  } else if (a.total_k <= 0) {
+    return false;
+  }
+  return true;
+}
+
+int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream) {
+  switch (a.group) {
+    case 1: return launch<1>(a, stream);
+    case 2: return launch<2>(a, stream);
+    case 4: return launch<4>(a, stream);
+    default: return launch<8>(a, stream);
+  }
+}
+
+}  // namespace pkv

@@ -155,6 +155,7 @@ def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_se
         _need(v_cache, "v_cache", dtype=q.dtype, ndim=4)
         nb, bs, hkv, _ = k_cache.shape
         mb = block_tables.shape[1]
+        total_k = 0
         if block_tables.shape[0] != B:
             raise ValueError("block_tables rows must equal the batch")
     else:
@@ -164,13 +165,16 @@ def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_se
         _need(v, "v", dtype=q.dtype, ndim=3)
         hkv = k.shape[1]
         nb = bs = mb = 0
+        total_k = k.shape[0]
+        if v.shape != k.shape:
+            raise ValueError("k and v shapes differ")
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", dtype=q.dtype)
     st = _lib.load().pkv_paged_varlen_prefill_attn(
         _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
-        _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables), mb, B, hq, hkv, d,
-        bs, nb, ctypes.c_float(scale), 1 if causal else 0, _dtype_code(q), _stream(stream))
+        _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables), mb, B, total_q,
+        total_k, hq, hkv, d, bs, nb, ctypes.c_float(scale), 1 if causal else 0, _dtype_code(q), _stream(stream))
     _lib.check("pkv_paged_varlen_prefill_attn", st)
     return out
 

@@ -127,9 +127,17 @@ def test_argument_errors_return_status():
                           2, 128, _lib.BF16, s)
     assert st == _lib.EALIGN
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
-                                           bt.data_ptr(), 1, 1, None, 0, 1, 4, 2, 64, 16, 4, ctypes.c_float(0.1), 1,
-                                           _lib.BF16, s)
+                                           bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 64, 16, 4,
+                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
     assert st == _lib.EUNSUPPORTED
+    st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
+                                           bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 128, 16, 4,
+                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
+    assert st == _lib.EINVAL  # no block tables and no packed k / v
+    st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
+                                           bt.data_ptr(), 1, 1, None, 0, 1, -1, 0, 4, 2, 128, 16, 4,
+                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
+    assert st == _lib.EINVAL
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 

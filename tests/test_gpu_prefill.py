@@ -22,7 +22,7 @@ def test_qwen3_prefill_prefix_chunk_poisoned():
 
 
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-@pytest.mark.parametrize("block_size", [16, 256])
+@pytest.mark.parametrize("block_size", [4, 8, 16, 24, 64, 256])
 def test_prefill_groups_and_block_sizes(group, block_size):
     w = wl.random_prefill(group * 10 + block_size, batch=5, max_new=150, min_new=1, max_cached_blocks=3,
                           block_size=block_size, num_q_heads=2 * group, num_kv_heads=2, head_dim=128)
