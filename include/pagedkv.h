@@ -209,7 +209,7 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *   total_q, total_k rows of q/out and of the packed k/v (total_k is ignored with block_tables)
  *   causal          1 = causal (bottom-right), 0 = full
  * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.  Block sizes that are a
- * multiple of 128, or a divisor of 128 of at least 8, and the packed path run on
+ * multiple of 64, or a divisor of 64 of at least 8, and the packed path run on
  * the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel.
  */
 int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const void* v,

@@ -9,7 +9,7 @@
 // How: a CTA owns one (query tile, sequence, KV head).  The tile's 128 rows
 // are (token, query head of the KV group) pairs, token-major, so one TMA box
 // of q [total_q, Hq, D] covers them and every K/V tile serves all G heads.
-//   warp 0     TMA producer: Q once, then K and V tiles of 128 keys into a
+//   warp 0     TMA producer: Q once, then K and V tiles of 64 keys into a
 //              2-stage ring (128-byte swizzled, one box per 64-wide d slab;
 //              paged tiles are gathered block piece by block piece).
 //   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (two S buffers so
@@ -19,6 +19,8 @@
 //              row max, exp2, bf16 P written back over its S buffer; O is
 //              rescaled in TMEM only when the row max grows by more than 2^8;
 //              final normalisation and store.
+// Two CTAs share an SM (256 TMEM columns and ~98 KB of shared memory each),
+// so one CTA's tensor work and loads overlap the other's softmax.
 // Every wait is bounded; on a timeout the CTA records an error, skips the
 // remaining waits and still frees its TMEM.
 #include "prefill_args.cuh"
@@ -30,20 +32,36 @@ using namespace pkv;
 
 constexpr int kD = 128;
 constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBN = 64;  // keys per tile
 constexpr int kStages = 2;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;  // S buffers at columns 0 and 128, O at 256
+constexpr int kCtasPerSm = 2;  // two CTAs share an SM: one's MMA and loads hide the other's softmax
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 2 * kBN;  // S buffers at columns 0 and kBN, O (128 columns) after them
 constexpr uint32_t kSlabQ = kBM * 128;
 constexpr uint32_t kSlabKV = kBN * 128;
 constexpr uint32_t kTileQ = 2 * kSlabQ;
 constexpr uint32_t kTileKV = 2 * kSlabKV;
 constexpr uint32_t kBarOffset = kTileQ + 2 * kStages * kTileKV;
 constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
+static_assert(kColO + kD <= kTmemCols, "TMEM plan exceeds the allocation");
 constexpr float kRescaleLog2 = 8.0f;
 
-enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, P_FULL = 9, O_DONE = 11, NUM_BARS = 12 };
+// O_DONE completes once per P.V product; it is waited only one phase behind
+// (lazy rescale).  O_FINAL completes once, after the last P.V: the epilogue and
+// teardown wait on it, because a parity wait on O_DONE could not tell the last
+// phase from one two phases earlier.
+enum Bar {
+  Q_FULL = 0,
+  K_FULL = 1,
+  V_FULL = 3,
+  KV_EMPTY = 5,
+  S_FULL = 7,
+  P_FULL = 9,
+  O_DONE = 11,
+  O_FINAL = 12,
+  NUM_BARS = 13
+};
 
 struct TcParams {
   __nv_bfloat16* out;
@@ -78,7 +96,7 @@ struct Waiter {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   constexpr int TQ = kBM / G;
@@ -127,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[P_FULL + b], 128);
     }
     mbar_init(&bars[O_DONE], 1);
+    mbar_init(&bars[O_FINAL], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -201,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait(&bars[K_FULL + st], (j / kStages) & 1);
         tc::fence_after_sync();
         const uint32_t k_addr = smem_u32(sk + st * kTileKV);
-        const uint32_t d = tmem + (j & 1) * 128;
+        const uint32_t d = tmem + (j & 1) * kBN;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlabQ + (kk & 3) * 32;
@@ -219,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait(&bars[V_FULL + st], (j / kStages) & 1);
         tc::fence_after_sync();
         const uint32_t v_addr = smem_u32(sv + st * kTileKV);
-        const uint32_t pcol = tmem + (j & 1) * 128;
+        const uint32_t pcol = tmem + (j & 1) * kBN;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = tc::smem_desc(v_addr + kk * 16 * 128, kSlabKV, 1024);
@@ -228,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&bars[KV_EMPTY + st]);
         tc::commit(&bars[O_DONE]);
       }
-      // the epilogue waits for the last P.V; wait here too so no MMA is in flight at teardown
-      wait(&bars[O_DONE], (n_tiles - 1) & 1);
+      tc::commit(&bars[O_FINAL]);
+      // no MMA may be in flight when TMEM is freed
+      wait(&bars[O_FINAL], 0);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -243,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
     float m_run = -INFINITY;
     float l_run = 0.f;
-    uint32_t r[128];
+    uint32_t r[kBN];
 
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
@@ -265,12 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(&bars[S_FULL + b], (j >> 1) & 1);
       tc::fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(lane_addr + b * 128 + c * 32, r + c * 32);
+      for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(lane_addr + b * kBN + c * 32, r + c * 32);
       tc::tmem_wait_ld();
       const bool need_mask = key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1);
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
+      for (int c = 0; c < kBN; ++c) {
         float x = __uint_as_float(r[c]) * p.scale_log2;
         if (need_mask && key0 + c > lim) x = -INFINITY;
         r[c] = __float_as_uint(x);
@@ -301,21 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P = exp2(s - m) rounded to bf16, packed two per column over the S buffer;
       // the row sum adds the same rounded values
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < kBN / 2; ++c) {
         const float p0 = exp2f(__uint_as_float(r[2 * c]) - m_use);
         const float p1 = exp2f(__uint_as_float(r[2 * c + 1]) - m_use);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         l_run += __low2float(pb) + __high2float(pb);
         r[c] = *reinterpret_cast<const uint32_t*>(&pb);
       }
-      tc::tmem_st32(lane_addr + b * 128, r);
-      tc::tmem_st32(lane_addr + b * 128 + 32, r + 32);
+#pragma unroll
+      for (int c = 0; c < kBN / 64; ++c) tc::tmem_st32(lane_addr + b * kBN + c * 32, r + c * 32);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&bars[P_FULL + b]);
     }
 
-    wait(&bars[O_DONE], (n_tiles - 1) & 1);
+    wait(&bars[O_FINAL], 0);
     tc::fence_after_sync();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     __nv_bfloat16* dst =

@@ -94,3 +94,15 @@ def test_decode_equals_prefill_single_row():
                                         block_tables=gp["block_tables"])
     torch.cuda.synchronize()
     assert (dec.float() - pre.float()).abs().max().item() <= 1e-2
+
+
+def test_prefill_many_short_sequences_repeated():
+    # hundreds of CTAs, two per SM: the tensor pipe runs behind the softmax, which is
+    # when a premature completion wait would read O before its last P.V landed
+    bs, nq, cached, B = 256, 64, 64, 400
+    rng = np.random.default_rng(17)
+    perm = rng.permutation(B + 8).tolist()
+    tables = [[perm[i]] for i in range(B)]
+    w = wl.PrefillWorkload("many-short", 23, 4, 2, 128, bs, B + 8, torch.bfloat16, [cached] * B, [nq] * B, tables)
+    for _ in range(3):
+        run_prefill(w)
