@@ -51,16 +51,20 @@ constexpr float kRescaleLog2 = 8.0f;
 // (lazy rescale).  O_FINAL completes once, after the last P.V: the epilogue and
 // teardown wait on it, because a parity wait on O_DONE could not tell the last
 // phase from one two phases earlier.
+// K and V stages are released separately: a K stage as soon as its Q K^T
+// completes, a V stage when its P V completes, so the producer keeps K two
+// tiles ahead of the tensor pipe.
 enum Bar {
   Q_FULL = 0,
   K_FULL = 1,
   V_FULL = 3,
-  KV_EMPTY = 5,
-  S_FULL = 7,
-  P_FULL = 9,
-  O_DONE = 11,
-  O_FINAL = 12,
-  NUM_BARS = 13
+  K_EMPTY = 5,
+  V_EMPTY = 7,
+  S_FULL = 9,
+  P_FULL = 11,
+  O_DONE = 13,
+  O_FINAL = 14,
+  NUM_BARS = 15
 };
 
 struct TcParams {
@@ -100,9 +104,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   constexpr int TQ = kBM / G;
-  const int seq = blockIdx.y;
-  const int g = blockIdx.z;
-  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
+  // blocks launch in linear order: x runs over (sequence, KV head), y over
+  // query tiles from the last (most keys under the causal mask) to the first
+  const int seq = blockIdx.x / p.hkv;
+  const int g = blockIdx.x % p.hkv;
+  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.y);
   const int q_begin = __ldg(p.cu_q + seq);
   const int nq = __ldg(p.cu_q + seq + 1) - q_begin;
   const int k_begin = __ldg(p.cu_k + seq);
@@ -138,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[K_FULL + s], 1);
       mbar_init(&bars[V_FULL + s], 1);
-      mbar_init(&bars[KV_EMPTY + s], 1);
+      mbar_init(&bars[K_EMPTY + s], 1);
+      mbar_init(&bars[V_EMPTY + s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[S_FULL + b], 1);
@@ -169,12 +176,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tc::tma_load_3d(sq + kSlabQ, &tm_q, 64, g * G, q_begin + tok0, &bars[Q_FULL]);
       mbar_arrive(&bars[Q_FULL]);
       const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-      for (int j = 0; j < n_tiles; ++j) {
+      // Loads one tile's K (is_v = false) or V into stage j % kStages, after the
+      // stage's previous occupant (tile j - kStages) was released.
+      auto load_tile = [&](int j, bool is_v) {
         const int st = j % kStages;
         const int use = j / kStages;
-        if (use > 0) wait(&bars[KV_EMPTY + st], (use - 1) & 1);
-        unsigned char* kd = sk + st * kTileKV;
-        unsigned char* vd = sv + st * kTileKV;
+        uint64_t* full = &bars[(is_v ? V_FULL : K_FULL) + st];
+        if (use > 0) wait(&bars[(is_v ? V_EMPTY : K_EMPTY) + st], (use - 1) & 1);
+        unsigned char* dst = (is_v ? sv : sk) + st * kTileKV;
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         const int key0 = j * kBN;
         if (p.paged) {
           const uint32_t piece_bytes = p.piece_rows * 128u;
@@ -188,36 +198,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               continue;
             }
             const int row = phys * p.block_size + (key - blk * p.block_size);
-            mbar_expect_tx(&bars[K_FULL + st], 2 * piece_bytes);
-            tc::tma_load_3d(kd + r * 128, &tm_k, 0, g, row, &bars[K_FULL + st]);
-            tc::tma_load_3d(kd + kSlabKV + r * 128, &tm_k, 64, g, row, &bars[K_FULL + st]);
-            mbar_expect_tx(&bars[V_FULL + st], 2 * piece_bytes);
-            tc::tma_load_3d(vd + r * 128, &tm_v, 0, g, row, &bars[V_FULL + st]);
-            tc::tma_load_3d(vd + kSlabKV + r * 128, &tm_v, 64, g, row, &bars[V_FULL + st]);
+            mbar_expect_tx(full, 2 * piece_bytes);
+            tc::tma_load_3d(dst + r * 128, map, 0, g, row, full);
+            tc::tma_load_3d(dst + kSlabKV + r * 128, map, 64, g, row, full);
           }
         } else {
           const int row = k_begin + key0;
-          mbar_expect_tx(&bars[K_FULL + st], kTileKV);
-          tc::tma_load_3d(kd, &tm_k, 0, g, row, &bars[K_FULL + st]);
-          tc::tma_load_3d(kd + kSlabKV, &tm_k, 64, g, row, &bars[K_FULL + st]);
-          mbar_expect_tx(&bars[V_FULL + st], kTileKV);
-          tc::tma_load_3d(vd, &tm_v, 0, g, row, &bars[V_FULL + st]);
-          tc::tma_load_3d(vd + kSlabKV, &tm_v, 64, g, row, &bars[V_FULL + st]);
+          mbar_expect_tx(full, kTileKV);
+          tc::tma_load_3d(dst, map, 0, g, row, full);
+          tc::tma_load_3d(dst + kSlabKV, map, 64, g, row, full);
         }
-        mbar_arrive(&bars[K_FULL + st]);
-        mbar_arrive(&bars[V_FULL + st]);
+        mbar_arrive(full);
+      };
+      // issue order K0, K1, V0, K2, V1, K3, ...: K runs two tiles ahead
+      for (int j = 0; j < kStages && j < n_tiles; ++j) load_tile(j, false);
+      for (int j = 0; j < n_tiles; ++j) {
+        load_tile(j, true);
+        if (j + kStages < n_tiles) load_tile(j + kStages, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
-      const uint32_t q_addr = smem_u32(sq);
-      wait(&bars[Q_FULL], 0);
-      auto issue_qk = [&](int j) {
-        const int st = j % kStages;
-        wait(&bars[K_FULL + st], (j / kStages) & 1);
+    // The whole warp follows the loop and waits every barrier phase in order;
+    // lane 0 issues the tensor-core work.
+    constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
+    constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
+    const uint32_t q_addr = smem_u32(sq);
+    wait(&bars[Q_FULL], 0);
+    auto issue_qk = [&](int j) {
+      const int st = j % kStages;
+      wait(&bars[K_FULL + st], (j / kStages) & 1);
+      if (lane == 0) {
         tc::fence_after_sync();
         const uint32_t k_addr = smem_u32(sk + st * kTileKV);
         const uint32_t d = tmem + (j & 1) * kBN;
@@ -229,28 +240,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           tc::mma_ss(d, a, b, idesc_qk, kk > 0);
         }
         tc::commit(&bars[S_FULL + (j & 1)]);
-      };
-      issue_qk(0);
-      for (int j = 0; j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) issue_qk(j + 1);
-        const int st = j % kStages;
-        wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
-        wait(&bars[V_FULL + st], (j / kStages) & 1);
+        tc::commit(&bars[K_EMPTY + st]);
+      }
+      __syncwarp();
+    };
+    issue_qk(0);
+    for (int j = 0; j < n_tiles; ++j) {
+      if (j + 1 < n_tiles) issue_qk(j + 1);
+      const int st = j % kStages;
+      wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
+      wait(&bars[V_FULL + st], (j / kStages) & 1);
+      unsigned char* vt = sv + st * kTileKV;
+      const int key0 = j * kBN;
+      if (key0 + kBN > nk) {
+        // V rows past the last key hold whatever their block had there (or were
+        // not loaded): zero them so 0 * stale never reaches O
+        const int first = nk - key0;
+        for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
+          const int rr = first + idx / 16;
+          const int ch = idx % 16;
+          *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) {
         tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(sv + st * kTileKV);
+        const uint32_t v_addr = smem_u32(vt);
         const uint32_t pcol = tmem + (j & 1) * kBN;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t b = tc::smem_desc(v_addr + kk * 16 * 128, kSlabKV, 1024);
           tc::mma_ts(tmem + kColO, pcol + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::commit(&bars[KV_EMPTY + st]);
+        tc::commit(&bars[V_EMPTY + st]);
         tc::commit(&bars[O_DONE]);
       }
-      tc::commit(&bars[O_FINAL]);
-      // no MMA may be in flight when TMEM is freed
-      wait(&bars[O_FINAL], 0);
+      __syncwarp();
     }
+    if (lane == 0) tc::commit(&bars[O_FINAL]);
+    // no MMA may be in flight when TMEM is freed
+    wait(&bars[O_FINAL], 0);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;
@@ -268,20 +298,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
       const int key0 = j * kBN;
-      if (key0 + kBN > nk) {
-        // rows of this V tile past the last key hold whatever the block had
-        // there (or nothing was loaded): zero them so 0 * stale never reaches O
-        const int st = j % kStages;
-        wait(&bars[V_FULL + st], (j / kStages) & 1);
-        unsigned char* vt = sv + st * kTileKV;
-        const int first = nk - key0;
-        for (int idx = (warp - 2) * 32 + lane; idx < (kBN - first) * 16; idx += 128) {
-          const int rr = first + idx / 16;
-          const int ch = idx % 16;
-          *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
       wait(&bars[S_FULL + b], (j >> 1) & 1);
       tc::fence_after_sync();
 #pragma unroll
@@ -399,7 +415,7 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
       cudaSuccess)
     return PKV_ECUDA;
-  dim3 grid(p.q_tiles, a.batch, a.hkv);
+  dim3 grid(a.batch * a.hkv, p.q_tiles);
   kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
