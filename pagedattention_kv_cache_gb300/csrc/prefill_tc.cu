@@ -99,6 +99,35 @@ struct Waiter {
   }
 };
 
+// exp2(scale * s - m) for two scores (fma on the f32x2 pair, ex2.approx per
+// element), rounded to bf16 and packed low = first.
+__device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, float scale, float neg_m) {
+  uint32_t out;
+  asm("{\n\t.reg .b64 x, c, m;\n\t.reg .f32 a, b;\n\t"
+      "mov.b64 x, {%1, %2};\n\t"
+      "mov.b64 c, {%3, %3};\n\t"
+      "mov.b64 m, {%4, %4};\n\t"
+      "fma.rn.f32x2 x, x, c, m;\n\t"
+      "mov.b64 {a, b}, x;\n\t"
+      "ex2.approx.ftz.f32 a, a;\n\t"
+      "ex2.approx.ftz.f32 b, b;\n\t"
+      "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
+      : "=r"(out)
+      : "r"(s0), "r"(s1), "f"(scale), "f"(neg_m));
+  return out;
+}
+
+// acc (two f32 lanes) += the two bf16 of w, widened exactly.
+__device__ __forceinline__ void add_bf16x2(uint64_t& acc, uint32_t w) {
+  asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 v;\n\t"
+      "shl.b32 lo, %1, 16;\n\t"
+      "and.b32 hi, %1, 0xffff0000;\n\t"
+      "mov.b64 v, {lo, hi};\n\t"
+      "add.rn.f32x2 %0, %0, v;\n\t}"
+      : "+l"(acc)
+      : "r"(w));
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -304,15 +333,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(lane_addr + b * kBN + c * 32, r + c * 32);
       tc::tmem_wait_ld();
       const bool need_mask = key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1);
+      // row maximum of the raw scores; the scale (> 0) is applied after
       float mt = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        float x = __uint_as_float(r[c]) * p.scale_log2;
-        if (need_mask && key0 + c > lim) x = -INFINITY;
-        r[c] = __float_as_uint(x);
-        mt = fmaxf(mt, x);
+        for (int c = 0; c < kBN; ++c) {
+          if (key0 + c > lim) r[c] = __float_as_uint(-INFINITY);
+          mt = fmaxf(mt, __uint_as_float(r[c]));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, __uint_as_float(r[c]));
       }
-      const float m_new = fmaxf(m_run, mt);
+      const float m_new = fmaxf(m_run, mt * p.scale_log2);
       const bool grow = m_new > m_run + kRescaleLog2 || (m_run == -INFINITY && m_new != -INFINITY);
       if (__any_sync(0xffffffffu, grow)) {
         const float factor = (m_run == -INFINITY || m_new <= m_run) ? 1.f : exp2f(m_run - m_new);
@@ -334,16 +367,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m_run = fmaxf(m_run, m_new);
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      // P = exp2(s - m) rounded to bf16, packed two per column over the S buffer;
-      // the row sum adds the same rounded values
+      // P = exp2(scale * s - m) rounded to bf16, packed two per column over the
+      // S buffer; the row sum adds the same rounded values (two lanes at a time)
+      uint64_t l_pair = 0;
 #pragma unroll
       for (int c = 0; c < kBN / 2; ++c) {
-        const float p0 = exp2f(__uint_as_float(r[2 * c]) - m_use);
-        const float p1 = exp2f(__uint_as_float(r[2 * c + 1]) - m_use);
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        l_run += __low2float(pb) + __high2float(pb);
-        r[c] = *reinterpret_cast<const uint32_t*>(&pb);
+        const uint32_t w = exp2_pair_bf16(r[2 * c], r[2 * c + 1], p.scale_log2, -m_use);
+        add_bf16x2(l_pair, w);
+        r[c] = w;
       }
+      l_run += __uint_as_float(static_cast<uint32_t>(l_pair)) + __uint_as_float(static_cast<uint32_t>(l_pair >> 32));
 #pragma unroll
       for (int c = 0; c < kBN / 64; ++c) tc::tmem_st32(lane_addr + b * kBN + c * 32, r + c * 32);
       tc::tmem_wait_st();
