@@ -152,6 +152,37 @@ int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const v
                           size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
 
 /*
+ * paged_verify_attn: the target pass of speculative decoding ("Warmup Guide --
+ * Inference Serving Internals", chapter 7: the target scores all drafted
+ * positions in one parallel pass).  Each sequence b has q_len query tokens,
+ * the last q_len positions of its context (their K/V stored first with
+ * pkv_kv_store, as decode stores its one new token).  Query token i of
+ * sequence b sits at position T - q_len + i (T = context_lens[b]) and attends
+ * cached tokens 0 .. T - q_len + i:
+ *   out[b, i, h, :] = sum_{t <= T - q_len + i} softmax(scale * q[b, i, h, :] . K_t) V_t
+ * with K_t / V_t gathered through block_tables as in paged_decode_attn.
+ * q_len == 1 is paged_decode_attn.
+ *
+ *   out, q          device, [batch, q_len, num_q_heads, head_dim]
+ *   context_lens    device, int32 [batch]; each is 0 (padding row: zeros, nothing
+ *                   read) or in [q_len, max_blocks_per_seq * block_size]; a value
+ *                   in [1, q_len) raises PKV_DERR_LEN_RANGE and the row reads nothing
+ *   workspace       as for paged_decode_attn, sized by
+ *                   pkv_paged_decode_workspace_bytes(batch, q_len * num_q_heads,
+ *                   head_dim, num_splits)
+ *   other arguments as for paged_decode_attn.
+ * Supported: BF16, head_dim 128, G in {1, 2, 4, 8} with G * q_len <= 8,
+ * num_kv_heads in [1, 8].
+ */
+int pkv_paged_verify_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, int32_t batch, int32_t q_len,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, float scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                          pkv_stream_t stream);
+
+/*
  * paged_decode_attn without a caller-provided workspace (no counterpart in the
  * pages: it is an addition of this library).
  *

@@ -13,7 +13,8 @@ from .ops import (  # noqa: F401
     kv_store,
     paged_decode_attn,
     paged_varlen_prefill_attn,
+    paged_verify_attn,
 )
 
-__all__ = ["kv_store", "paged_decode_attn", "paged_varlen_prefill_attn", "decode_workspace",
+__all__ = ["kv_store", "paged_decode_attn", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
            "decode_workspace_bytes", "device_error", "metadata", "ops", "workloads"]

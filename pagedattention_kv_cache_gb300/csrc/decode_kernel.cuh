@@ -1,0 +1,638 @@
+// Paged decode / verify attention kernel shared by the decode entry points
+// (one query token per sequence, decode.cu) and the verify entry point (QL
+// query tokens per sequence, verify.cu).
+//
+//
+// What is computed ("3.6 ModelRunner, CUDA Graph, and benchmarks", section 2,
+// decode; section 5, padding rows): for sequence b and query head h reading
+// KV head g = h / G, over t < context_lens[b],
+//     s_t = scale * q[b, h] . K_t,  out[b, h] = sum_t softmax(s)_t V_t,
+// with K_t / V_t at physical block block_tables[b, t / bs], offset t % bs.
+// context_lens 0 writes zeros and reads nothing.
+//
+// How (GB300 design):
+//  * A CTA covers every KV head of a token range, so each token's K (or V)
+//    row of all heads, [Hkv, D], is contiguous in the [blocks, bs, Hkv, D]
+//    pool and a run of tokens inside one block is one contiguous span.  One
+//    producer lane streams those spans into a ring of shared-memory stages with
+//    1-D bulk (TMA) copies completed on mbarriers; every K/V byte is read from
+//    HBM exactly once, and all G query heads of a KV head reuse it on chip.
+//  * One consumer warp per (KV head, token phase).  Within a warp LPT lanes
+//    share a token (16-byte conflict-free shared loads, fp32 dot products,
+//    xor-shuffle reduction); scores of a stage are reduced to a stage maximum
+//    and folded into a running online softmax (exp2 domain), then P.V is
+//    accumulated in registers.
+//  * Split over the context: the batch's context tokens, flattened, are
+//    divided evenly over the grid (automatic mode) or each sequence into S
+//    equal parts.  A sequence covered by one CTA is written directly; otherwise
+//    each part writes (o, m, l) to the workspace and the last CTA to finish
+//    a sequence (atomic ticket, no waiting) merges the parts by log-sum-exp.
+//
+// Verify (speculative-decoding target pass, QL > 1): query token i of
+// sequence b sits at position context_lens[b] - QL + i and attends keys up to
+// it, so the QL tokens just stored are causally masked among themselves.  The
+// warp's rows become (query token, head) pairs; K/V are still read once.
+#pragma once
+
+#include <cfloat>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+using pkv::Chunk;
+
+constexpr int kMinTokensPerCta = 32;
+constexpr int kAutoCtasPerSm = 1;      // grid of the automatic split
+constexpr int kWorkspaceCtasPerSm = 2;  // workspace sized for up to this many CTAs per SM
+constexpr int kMaxStages = 4;
+constexpr int kSmemBudget = 200 * 1024;
+
+// Register shape of a consumer warp that holds R query rows (query heads x
+// query tokens) of one KV head.
+template <typename T, int D, int R>
+struct Shape {
+  static constexpr int EPC = Chunk<T>::N;                   // elements per 16-byte chunk
+  static constexpr int ROW_BYTES = D * static_cast<int>(sizeof(T));  // one head's row
+  static constexpr int CHUNKS = ROW_BYTES / 16;
+  static constexpr int EPL8 = (CHUNKS / 8) * EPC;
+  static constexpr int LPT = (R * EPL8 > 32 && CHUNKS >= 16) ? 16 : 8;  // lanes per token
+  static constexpr int CPL = CHUNKS / LPT;                  // chunks per lane
+  static constexpr int EPL = CPL * EPC;                     // elements per lane
+  static constexpr int TPW = 32 / LPT;                      // tokens per warp round
+  static constexpr int ROUNDS = (ROW_BYTES >= 512 || R >= 5) ? 2 : 4;  // rounds per stage per warp
+  static_assert(CPL >= 1, "head row too short for the lane split");
+};
+
+struct Params {
+  void* out;
+  const void* q;
+  const unsigned char* k_cache;
+  const unsigned char* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* part_o;     // [slots, QL * Hq, D]
+  float* part_ml;    // [slots, QL * Hq, 2]
+  int32_t* counters; // [batch]
+  unsigned int* err;
+  int max_blocks;
+  int batch;
+  int hq;  // query heads per query token
+  int ql;  // query tokens per sequence (1 = decode)
+  int hkv;
+  int block_size;
+  int num_blocks;
+  float scale_log2;  // scale * log2(e)
+  int num_splits;    // 0 = automatic
+  int nw;            // consumer warps
+  int wph;           // consumer warps per KV head
+  int t_stage;       // tokens per stage
+  int stages;
+  size_t stage_bytes;
+};
+
+// One contiguous piece of work: tokens [t0, t1) of sequence b.
+struct Segment {
+  int b;
+  int ctx;  // context length of sequence b
+  int t0, t1;
+  int nparts;      // CTAs sharing sequence b
+  int first_slot;  // workspace slot of the sequence's first part
+  int slot;        // this part's slot
+};
+
+// Bounded pipeline wait.  On a timeout the CTA raises PKV_DERR_WAIT_TIMEOUT,
+// sets its abort flag and carries on (all later waits return at once), so
+// every warp still reaches every named barrier and the kernel ends; the
+// results of an aborted CTA are invalid.
+__device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* err) {
+  if (*abort_flag) return;
+  if (!pkv::mbar_wait(bar, parity)) {
+    *abort_flag = 1;
+    pkv::raise_error(err, PKV_DERR_WAIT_TIMEOUT);
+  }
+}
+
+__device__ __forceinline__ int context_len(const Params& p, int b) {
+  const int n = __ldg(p.context_lens + b);
+  if (n < 0 || n > p.max_blocks * p.block_size || (n > 0 && n < p.ql)) {
+    pkv::raise_error(p.err, PKV_DERR_LEN_RANGE);
+    return 0;
+  }
+  return n;
+}
+
+// Work plan of this CTA, computed identically by every thread.
+struct Plan {
+  // automatic mode
+  long long start, end, per;
+  int b_first;
+  long long cu_first;
+  // fixed-split mode
+  Segment fixed;
+  bool fixed_valid;
+};
+
+// Block-wide sum over context lengths and search for the first sequence
+// overlapping this CTA's token range (automatic mode).
+__device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  long long local = 0;
+  for (int b = tid; b < p.batch; b += nthreads) local += context_len(p, b);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) local += __shfl_xor_sync(0xffffffffu, local, off);
+  if (tid % 32 == 0) sh[tid / 32] = local;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < nthreads / 32; ++w) total += sh[w];
+  __syncthreads();
+  const long long grid = gridDim.x;
+  long long per = (total + grid - 1) / grid;
+  if (per < kMinTokensPerCta) per = kMinTokensPerCta;
+  plan.per = per;
+  plan.start = per * blockIdx.x;
+  plan.end = plan.start + per < total ? plan.start + per : total;
+  plan.b_first = -1;
+  plan.cu_first = 0;
+  if (plan.start >= plan.end) return;
+  // chunked exclusive scan to locate the sequence containing token `start`
+  if (tid == 0) sh[32] = -1;
+  long long running = 0;
+  for (int base = 0; base < p.batch; base += nthreads) {
+    const int b = base + tid;
+    const long long n = b < p.batch ? context_len(p, b) : 0;
+    long long incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid % 32 >= off) incl += y;
+    }
+    if (tid % 32 == 31) sh[tid / 32] = incl;
+    __syncthreads();
+    long long warp_prefix = 0;
+    long long chunk_total = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      if (w < tid / 32) warp_prefix += sh[w];
+      chunk_total += sh[w];
+    }
+    const long long excl = running + warp_prefix + incl - n;
+    if (n > 0 && excl <= plan.start && plan.start < excl + n) {
+      sh[32] = b;
+      sh[33] = excl;
+    }
+    running += chunk_total;
+    __syncthreads();
+    if (sh[32] >= 0) break;
+  }
+  plan.b_first = static_cast<int>(sh[32]);
+  plan.cu_first = sh[33];
+  __syncthreads();
+}
+
+__device__ void plan_fixed(const Params& p, Plan& plan) {
+  const int S = p.num_splits;
+  const int b = blockIdx.x / S;
+  const int j = blockIdx.x % S;
+  plan.fixed_valid = false;
+  if (b >= p.batch) return;
+  const int n = context_len(p, b);
+  if (n == 0) return;
+  const int chunk = (n + S - 1) / S;
+  const int t0 = j * chunk;
+  if (t0 >= n) return;
+  const int t1 = t0 + chunk < n ? t0 + chunk : n;
+  plan.fixed = Segment{b, n, t0, t1, (n + chunk - 1) / chunk, b * S, b * S + j};
+  plan.fixed_valid = true;
+}
+
+// Calls fn(segment) for every segment of this CTA, in order.
+template <typename Fn>
+__device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& plan, Fn&& fn) {
+  if (p.num_splits > 0) {
+    if (plan.fixed_valid) return fn(plan.fixed);
+    return true;
+  }
+  if (plan.b_first < 0) return true;
+  long long cu = plan.cu_first;
+  for (int b = plan.b_first; b < p.batch && cu < plan.end; ++b) {
+    const int n = context_len(p, b);
+    if (n > 0) {
+      const long long s0 = plan.start > cu ? plan.start : cu;
+      const long long s1 = plan.end < cu + n ? plan.end : cu + n;
+      const int c0 = static_cast<int>(cu / plan.per);
+      const int c1 = static_cast<int>((cu + n - 1) / plan.per);
+      Segment seg{b, n, static_cast<int>(s0 - cu), static_cast<int>(s1 - cu), c1 - c0 + 1, c0 + b,
+                  static_cast<int>(blockIdx.x) + b};
+      if (!fn(seg)) return false;
+    }
+    cu += n;
+  }
+  return true;
+}
+
+// G query heads per KV head, QL query tokens per sequence.  A consumer warp
+// holds R = G * QL rows: row rho is query token rho / G, head g * G + rho % G.
+template <typename T, int D, int G, int QL>
+__global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
+  constexpr int R = G * QL;
+  using S = Shape<T, D, R>;
+  const int rows_per_seq = QL * p.hq;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+  const int nw = p.nw;
+
+  unsigned char* stage_base = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  long long* sh = reinterpret_cast<long long*>(empty + kMaxStages);  // 64 scratch words
+  int* sh_flag = reinterpret_cast<int*>(sh + 64);
+  float* merge = reinterpret_cast<float*>(sh_flag + 32);
+
+  volatile int* abort_flag = sh_flag + 1;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      pkv::mbar_init(&full[s], 1);
+      pkv::mbar_init(&empty[s], nw);
+    }
+    pkv::fence_mbar_init();
+  }
+
+  // context length 0 rows: zeros, nothing read (section 5 padding)
+  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+    if (context_len(p, b) != 0) continue;
+    T* o = static_cast<T*>(p.out) + static_cast<size_t>(b) * rows_per_seq * D;
+    for (int i = tid; i < rows_per_seq * D; i += blockDim.x) o[i] = static_cast<T>(0.0f);
+  }
+
+  Plan plan;
+  if (p.num_splits > 0) {
+    plan_fixed(p, plan);
+    __syncthreads();
+  } else {
+    plan_auto(p, plan, sh);
+  }
+
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t policy = pkv::l2_evict_first_policy();
+    const size_t head_row = static_cast<size_t>(p.hkv) * S::ROW_BYTES;  // bytes per token, all heads
+    int it = 0;
+    for_each_segment(p, plan, [&](const Segment& seg) -> bool {
+      const int32_t* table = p.block_tables + static_cast<size_t>(seg.b) * p.max_blocks;
+      for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
+        const int s = it % p.stages;
+        const uint32_t use = it / p.stages;
+        if (use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
+        const int nt = min(p.t_stage, seg.t1 - t);
+        unsigned char* ks = stage_base + s * p.stage_bytes;
+        unsigned char* vs = ks + p.stage_bytes / 2;
+        for (int tt = t; tt < t + nt;) {
+          const int blk = tt / p.block_size;
+          const int off = tt - blk * p.block_size;
+          const int n = min(p.block_size - off, t + nt - tt);
+          const int phys = __ldg(table + blk);
+          if (phys < 0 || phys >= p.num_blocks) {
+            pkv::raise_error(p.err, PKV_DERR_BLOCK_RANGE);
+          } else {
+            const size_t src = (static_cast<size_t>(phys) * p.block_size + off) * head_row;
+            const size_t dst = static_cast<size_t>(tt - t) * head_row;
+            const uint32_t bytes = static_cast<uint32_t>(n * head_row);
+            pkv::mbar_expect_tx(&full[s], 2 * bytes);
+            pkv::bulk_g2s(ks + dst, p.k_cache + src, bytes, &full[s], policy);
+            pkv::bulk_g2s(vs + dst, p.v_cache + src, bytes, &full[s], policy);
+          }
+          tt += n;
+        }
+        pkv::mbar_arrive(&full[s]);
+      }
+      return true;
+    });
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = warp % p.hkv;
+  const int phase = warp / p.hkv;
+  const int tg = lane / S::LPT;   // token group inside the warp
+  const int lig = lane % S::LPT;  // lane inside the token group
+  const int nthreads_c = nw * 32;
+  int it = 0;
+
+  for_each_segment(p, plan, [&](const Segment& seg) -> bool {
+    // q of the R rows sharing KV head g, pre-scaled into the exp2 domain
+    float qr[R][S::EPL];
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+      const T* qh =
+          static_cast<const T*>(p.q) + ((static_cast<size_t>(seg.b) * QL + h / G) * p.hq + g * G + h % G) * D;
+#pragma unroll
+      for (int k = 0; k < S::CPL; ++k) {
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(qh) + lig + S::LPT * k);
+        Chunk<T>::unpack(c, &qr[h][k * S::EPC]);
+      }
+#pragma unroll
+      for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
+    }
+    float acc[R][S::EPL];
+    float m[R], l[R];
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < S::EPL; ++e) acc[h][e] = 0.f;
+    }
+
+    for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
+      const int s = it % p.stages;
+      const uint32_t use = it / p.stages;
+      wait_or_abort(&full[s], use & 1u, abort_flag, p.err);
+      const int nt = min(p.t_stage, seg.t1 - t);
+      const unsigned char* ks = stage_base + s * p.stage_bytes;
+      const unsigned char* vs = ks + p.stage_bytes / 2;
+
+      float sc[S::ROUNDS][R];
+#pragma unroll
+      for (int r = 0; r < S::ROUNDS; ++r) {
+        const int tt = (r * p.wph + phase) * S::TPW + tg;
+        const bool valid = tt < nt;
+        float dot[R];
+#pragma unroll
+        for (int h = 0; h < R; ++h) dot[h] = 0.f;
+        if (valid) {
+          const unsigned char* row = ks + (static_cast<size_t>(tt) * p.hkv + g) * S::ROW_BYTES;
+#pragma unroll
+          for (int k = 0; k < S::CPL; ++k) {
+            float f[S::EPC];
+            Chunk<T>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+#pragma unroll
+            for (int h = 0; h < R; ++h)
+#pragma unroll
+              for (int e = 0; e < S::EPC; ++e) dot[h] = fmaf(qr[h][k * S::EPC + e], f[e], dot[h]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < R; ++h) {
+#pragma unroll
+          for (int off = 1; off < S::LPT; off <<= 1) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+          // query token h / G sits at position ctx - QL + h / G and sees keys up to it
+          const bool visible = QL == 1 || t + tt <= seg.ctx - QL + h / G;
+          sc[r][h] = (valid && visible) ? dot[h] : -INFINITY;
+        }
+      }
+
+      // fold the stage into the running softmax state
+#pragma unroll
+      for (int h = 0; h < R; ++h) {
+        float mt = sc[0][h];
+#pragma unroll
+        for (int r = 1; r < S::ROUNDS; ++r) mt = fmaxf(mt, sc[r][h]);
+#pragma unroll
+        for (int off = S::LPT; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+        const float mnew = fmaxf(m[h], mt);
+        if (mnew == -INFINITY) {
+#pragma unroll
+          for (int r = 0; r < S::ROUNDS; ++r) sc[r][h] = 0.f;
+          continue;
+        }
+        if (mnew != m[h]) {
+          const float corr = exp2f(m[h] - mnew);
+          l[h] *= corr;
+#pragma unroll
+          for (int e = 0; e < S::EPL; ++e) acc[h][e] *= corr;
+          m[h] = mnew;
+        }
+#pragma unroll
+        for (int r = 0; r < S::ROUNDS; ++r) {
+          const float pr = exp2f(sc[r][h] - mnew);
+          l[h] += pr;
+          sc[r][h] = pr;
+        }
+      }
+
+#pragma unroll
+      for (int r = 0; r < S::ROUNDS; ++r) {
+        const int tt = (r * p.wph + phase) * S::TPW + tg;
+        if (tt < nt) {
+          const unsigned char* row = vs + (static_cast<size_t>(tt) * p.hkv + g) * S::ROW_BYTES;
+#pragma unroll
+          for (int k = 0; k < S::CPL; ++k) {
+            float f[S::EPC];
+            Chunk<T>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+#pragma unroll
+            for (int h = 0; h < R; ++h)
+#pragma unroll
+              for (int e = 0; e < S::EPC; ++e) acc[h][k * S::EPC + e] = fmaf(sc[r][h], f[e], acc[h][k * S::EPC + e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) pkv::mbar_arrive(&empty[s]);
+    }
+
+    // reduce the token groups of the warp (m is already warp-uniform)
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+#pragma unroll
+      for (int off = S::LPT; off < 32; off <<= 1) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+      }
+    }
+
+    // merge the warps that share KV head g (token phases)
+    if (p.wph > 1) {
+      const int rec = D + 2;
+      if (tg == 0) {
+#pragma unroll
+        for (int h = 0; h < R; ++h) {
+          float* dstm = merge + (static_cast<size_t>(warp) * R + h) * rec;
+#pragma unroll
+          for (int k = 0; k < S::CPL; ++k)
+#pragma unroll
+            for (int e = 0; e < S::EPC; ++e) dstm[(lig + S::LPT * k) * S::EPC + e] = acc[h][k * S::EPC + e];
+          if (lig == 0) {
+            dstm[D] = m[h];
+            dstm[D + 1] = l[h];
+          }
+        }
+      }
+      pkv::named_barrier_sync(1, nthreads_c);
+      if (phase == 0) {
+#pragma unroll
+        for (int h = 0; h < R; ++h) {
+          float mm = m[h];
+          for (int ph = 1; ph < p.wph; ++ph) mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + h) * rec + D]);
+          const float w0 = mm == -INFINITY ? 0.f : exp2f(m[h] - mm);
+          float ll = l[h] * w0;
+#pragma unroll
+          for (int e = 0; e < S::EPL; ++e) acc[h][e] *= w0;
+          for (int ph = 1; ph < p.wph; ++ph) {
+            const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + h) * rec;
+            const float mw = src[D];
+            const float w = mw == -INFINITY ? 0.f : exp2f(mw - mm);
+            ll += w * src[D + 1];
+#pragma unroll
+            for (int k = 0; k < S::CPL; ++k)
+#pragma unroll
+              for (int e = 0; e < S::EPC; ++e)
+                acc[h][k * S::EPC + e] += w * src[(lig + S::LPT * k) * S::EPC + e];
+          }
+          m[h] = mm;
+          l[h] = ll;
+        }
+      }
+      pkv::named_barrier_sync(1, nthreads_c);
+    }
+
+    // write the result (whole sequence) or this part's state
+    if (phase == 0 && tg == 0) {
+#pragma unroll
+      for (int h = 0; h < R; ++h) {
+        const int head = (h / G) * p.hq + g * G + h % G;  // row within the sequence's QL * Hq rows
+        if (seg.nparts == 1) {
+          const float inv = 1.f / l[h];
+          T* o = static_cast<T*>(p.out) + (static_cast<size_t>(seg.b) * rows_per_seq + head) * D;
+#pragma unroll
+          for (int k = 0; k < S::CPL; ++k) {
+            float f[S::EPC];
+#pragma unroll
+            for (int e = 0; e < S::EPC; ++e) f[e] = acc[h][k * S::EPC + e] * inv;
+            reinterpret_cast<uint4*>(o)[lig + S::LPT * k] = Chunk<T>::pack(f);
+          }
+        } else {
+          float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
+#pragma unroll
+          for (int k = 0; k < S::CPL; ++k)
+#pragma unroll
+            for (int e = 0; e < S::EPC; e += 4)
+              *reinterpret_cast<float4*>(po + (lig + S::LPT * k) * S::EPC + e) =
+                  make_float4(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], acc[h][k * S::EPC + e + 2],
+                              acc[h][k * S::EPC + e + 3]);
+          if (lig == 0)
+            *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
+                make_float2(m[h], l[h]);
+        }
+      }
+    }
+
+    if (seg.nparts > 1) {
+      // the last part to arrive merges all parts of the sequence
+      pkv::named_barrier_sync(1, nthreads_c);
+      if (tid == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(p.counters + seg.b, 1);
+        sh_flag[0] = ticket == seg.nparts - 1;
+      }
+      pkv::named_barrier_sync(1, nthreads_c);
+      if (sh_flag[0]) {
+        __threadfence();
+        T* o = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
+        for (int i = tid; i < rows_per_seq * D; i += nthreads_c) {
+          const int head = i / D;
+          float mm = -INFINITY;
+          for (int j = 0; j < seg.nparts; ++j)
+            mm = fmaxf(mm, __ldcg(p.part_ml + (static_cast<size_t>(seg.first_slot + j) * rows_per_seq + head) * 2));
+          float ll = 0.f, oo = 0.f;
+          for (int j = 0; j < seg.nparts; ++j) {
+            const size_t slot = seg.first_slot + j;
+            const float2 ml =
+                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * rows_per_seq + head) * 2));
+            const float w = exp2f(ml.x - mm);
+            ll += w * ml.y;
+            oo += w * __ldcg(p.part_o + slot * rows_per_seq * D + i);
+          }
+          o[i] = static_cast<T>(oo / ll);
+        }
+        if (tid == 0) p.counters[seg.b] = 0;
+      }
+      pkv::named_barrier_sync(1, nthreads_c);
+    }
+    return true;
+  });
+}
+
+// ------------------------------------------------------------------ host side
+
+struct LaunchShape {
+  int nw, wph, t_stage, stages;
+  size_t stage_bytes, smem;
+};
+
+template <typename T, int D, int R>
+LaunchShape launch_shape(int hkv) {
+  using S = Shape<T, D, R>;
+  LaunchShape ls;
+  ls.wph = hkv >= 8 ? 1 : 8 / hkv;
+  ls.nw = hkv * ls.wph;
+  ls.t_stage = S::ROUNDS * S::TPW * ls.wph;
+  ls.stage_bytes = static_cast<size_t>(ls.t_stage) * hkv * S::ROW_BYTES * 2;
+  const size_t misc = 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
+                      (ls.wph > 1 ? static_cast<size_t>(ls.nw) * R * (D + 2) * sizeof(float) : 0);
+  int stages = static_cast<int>((kSmemBudget - misc) / ls.stage_bytes);
+  ls.stages = stages > kMaxStages ? kMaxStages : stages;
+  ls.smem = ls.stages * ls.stage_bytes + misc;
+  return ls;
+}
+
+size_t slot_count(int batch, int num_splits, int sms) {
+  if (num_splits == 1) return 0;
+  if (num_splits > 1) return static_cast<size_t>(batch) * num_splits;
+  return static_cast<size_t>(sms) * kWorkspaceCtasPerSm + batch;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t workspace_layout(int batch, int hq, int d, int num_splits, int sms, size_t* off_o, size_t* off_ml) {
+  const size_t slots = slot_count(batch, num_splits, sms);
+  if (slots == 0) return 0;
+  const size_t counters = align256(static_cast<size_t>(batch) * sizeof(int32_t));
+  *off_o = counters;
+  *off_ml = counters + align256(slots * hq * d * sizeof(float));
+  return *off_ml + align256(slots * hq * 2 * sizeof(float));
+}
+
+template <typename T, int D, int G, int QL>
+int launch(Params& p, int sms, cudaStream_t stream) {
+  const LaunchShape ls = launch_shape<T, D, G * QL>(p.hkv);
+  if (ls.stages < 2) return PKV_EUNSUPPORTED;
+  p.nw = ls.nw;
+  p.wph = ls.wph;
+  p.t_stage = ls.t_stage;
+  p.stages = ls.stages;
+  p.stage_bytes = ls.stage_bytes;
+  auto kernel = paged_decode_kernel<T, D, G, QL>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ls.smem)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
+  unsigned grid;
+  if (p.num_splits > 0)
+    grid = static_cast<unsigned>(static_cast<long long>(p.batch) * p.num_splits);
+  else
+    grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
+  if (grid == 0) return PKV_OK;
+  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+template <typename T, int D>
+int dispatch_g(Params& p, int group, int sms, cudaStream_t stream) {
+  switch (group) {
+    case 1: return launch<T, D, 1, 1>(p, sms, stream);
+    case 2: return launch<T, D, 2, 1>(p, sms, stream);
+    case 4: return launch<T, D, 4, 1>(p, sms, stream);
+    case 8: return launch<T, D, 8, 1>(p, sms, stream);
+    default: return PKV_EUNSUPPORTED;
+  }
+}
+
+}  // namespace
+

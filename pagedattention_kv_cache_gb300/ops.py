@@ -112,6 +112,36 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     return out
 
 
+def paged_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *,
+                      num_splits: int = 0, workspace: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Speculative-decoding verify attention: q [B, q_len, Hq, D], the last q_len context
+    tokens of each sequence, each causally limited to its own position."""
+    _need(q, "q", ndim=4)
+    _need(k_cache, "k_cache", dtype=q.dtype, ndim=4)
+    _need(v_cache, "v_cache", dtype=q.dtype, ndim=4)
+    _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _need(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    B, ql, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes between q, caches, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=q.dtype)
+    if workspace is None:
+        workspace = decode_workspace(B, ql * hq, d, num_splits, device=q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().pkv_paged_verify_attn(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, ql, hq, hkv, d, bs, nb, ctypes.c_float(scale), num_splits, ws_ptr, ws_bytes,
+        _dtype_code(q), _stream(stream))
+    _lib.check("pkv_paged_verify_attn", st)
+    return out
+
+
 def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                               block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *,
                               num_splits: int = 0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

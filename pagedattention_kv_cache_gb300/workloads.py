@@ -268,3 +268,21 @@ def prefill_tensors(wl: PrefillWorkload, device="cpu", poison: bool = False) -> 
         _poison_unused(k_cache, wl.block_tables, wl.num_cached, wl.block_size)
         _poison_unused(v_cache, wl.block_tables, wl.num_cached, wl.block_size)
     return dict(q=q, k=k, v=v, k_cache=k_cache, v_cache=v_cache)
+
+
+def verify_tensors(wl: DecodeWorkload, q_len: int, device="cpu", layer: int = 0) -> dict:
+    """Draw the inputs of one speculative-decoding verify pass.
+
+    q [B, q_len, Hq, D] holds the last q_len positions of each context; k_new /
+    v_new [B * q_len, Hkv, D] are their K/V rows (sequence-major), to be stored
+    before attention; the caches hold the history as in decode_tensors.
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed * 1000 + 500 + layer)
+    B, Hq, Hkv, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    pool_shape = (wl.num_blocks, wl.block_size, Hkv, D)
+    return dict(q=_randn(gen, (B, q_len, Hq, D), device, wl.dtype),
+                k_new=_randn(gen, (B * q_len, Hkv, D), device, wl.dtype),
+                v_new=_randn(gen, (B * q_len, Hkv, D), device, wl.dtype),
+                k_cache=_randn(gen, pool_shape, device, wl.dtype),
+                v_cache=_randn(gen, pool_shape, device, wl.dtype))
