@@ -31,6 +31,10 @@ Pin status of each function (what fixes it other than itself; the tests under
   dominant logit), a textbook contiguous attention built from
   ``scipy.special.softmax`` and brute-force float64 loops on tiny shapes,
   and the block-permutation and prefix-hit invariants.
+* fp8.e4m3_encode / e4m3_decode / quantize / kv_store_fp8 (the reduced-precision
+  KV cache, a reading: OCP E4M3 with a per-tensor scale): pinned to code values
+  fixed by the format definition, round trips of every finite code, torch's
+  float8_e4m3fn conversion inside the finite range, saturation and ties to even.
 * attention.decode_partials / combine_partials: pinned by the identity that
   merging the partitions of a context reproduces attention over the whole
   context, and by a hand-computed two-partition example.
@@ -39,4 +43,4 @@ Pin status of each function (what fixes it other than itself; the tests under
   bits of float arithmetic is unpinned by design).
 """
 
-from . import attention, metadata  # noqa: F401
+from . import attention, fp8, metadata  # noqa: F401

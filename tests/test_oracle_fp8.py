@@ -1,0 +1,52 @@
+"""Pins for the oracle's E4M3 codec (CPU only): values fixed by the format's
+definition, round trips, torch's float8_e4m3fn conversion inside the finite
+range (a library routine), saturation, and ties to even."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8
+
+
+def test_decode_known_codes():
+    # (code, value) fixed by the format: bias 7, 3 mantissa bits, subnormals below 2^-6
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5,
+             0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, value in table.items():
+        assert fp8.e4m3_decode(np.uint8(code)) == value
+    assert np.isnan(fp8.e4m3_decode(np.uint8(0x7F))) and np.isnan(fp8.e4m3_decode(np.uint8(0xFF)))
+
+
+def test_every_finite_code_round_trips():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(fp8.e4m3_encode(fp8.e4m3_decode(codes)), codes)
+
+
+def test_matches_torch_float8_inside_the_finite_range():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000) * s for s in (0.01, 1.0, 30.0, 150.0)])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = fp8.e4m3_encode(x.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_saturation_and_nan():
+    assert fp8.e4m3_encode(500.0) == 0x7E
+    assert fp8.e4m3_encode(-1e9) == 0xFE
+    assert fp8.e4m3_encode(464.0) == 0x7E  # beyond the largest value, not rounded up to NaN
+    assert fp8.e4m3_encode(np.nan) == 0x7F
+
+
+@pytest.mark.parametrize("x,code", [(232.0, 0x76), (248.0, 0x78), (1.0625, 0x38), (1.1875, 0x3A),
+                                    (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02)])
+def test_ties_go_to_even(x, code):
+    # each x lies exactly halfway between two neighbours; the even code wins
+    assert fp8.e4m3_encode(x) == code
+
+
+def test_quantize_divides_in_float32():
+    x = np.float32(3.0)
+    assert fp8.quantize(x, 0.1) == fp8.e4m3_encode(np.float64(np.float32(3.0) / np.float32(0.1)))
+    assert fp8.dequantize(fp8.quantize(np.float32(1.0), 0.5), 0.5) == 1.0
