@@ -334,6 +334,122 @@ def bench_e2e(args, res, device, world):
             "ms_per_step": round(ms / args.steps, 4)}
 
 
+FP8_K_SCALE = 1.0 / 64
+FP8_V_SCALE = 1.0 / 64
+
+
+def decode_alg_bytes_fp8(w) -> int:
+    kv = sum(w.context_lens) * w.num_kv_heads * w.head_dim * 2  # one byte per element
+    qo = 2 * w.batch * w.num_q_heads * w.head_dim * 2  # bf16 q and out
+    meta = sum(-(-n // w.block_size) for n in w.context_lens) * 4 + w.batch * 4
+    return kv + qo + meta
+
+
+def bench_fp8(args, device, world):
+    """The same 28-layer decode step over an FP8 (E4M3) cache: quantizing store + decode."""
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b256_28l()
+    L = w.num_layers
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 7)
+    kc, vc, q, kn, vn = [], [], [], [], []
+    for _ in range(L):
+        for pool, scale in ((kc, FP8_K_SCALE), (vc, FP8_V_SCALE)):
+            x = torch.randn(shape, generator=gen, device=device)
+            pool.append((x / scale).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8))
+            del x
+        q.append(torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen, device=device).bfloat16())
+        kn.append(torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen, device=device).bfloat16())
+        vn.append(torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen, device=device).bfloat16())
+    meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+    out = [torch.empty_like(x) for x in q]
+    ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0, device=device)
+
+    def step(events=None):
+        for layer in range(L):
+            pkv.kv_store_fp8(kn[layer], vn[layer], kc[layer], vc[layer], meta["slot_mapping"], FP8_K_SCALE,
+                             FP8_V_SCALE)
+            if events is not None:
+                events[layer][0].record()
+            pkv.paged_decode_attn_fp8(q[layer], kc[layer], vc[layer], meta["block_tables"], meta["context_lens"],
+                                      w.scale, FP8_K_SCALE, FP8_V_SCALE, workspace=ws, out=out[layer])
+            if events is not None:
+                events[layer][1].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    start.record()
+    for k in range(args.steps):
+        step(ev[k])
+    stop.record()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    ms = max_over_ranks(start.elapsed_time(stop), world, device) / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for per in ev for (a, b) in per)
+    step_bytes = L * (decode_alg_bytes_fp8(w) + 2 * w.batch * w.num_kv_heads * w.head_dim * (2 + 1) + 4 * w.batch)
+    dec_bytes = decode_alg_bytes_fp8(w)
+    hbm_peak = measured_peaks()[0]
+    result = {"workload": w.name + "-fp8-e4m3", "ms_per_step": round(ms, 4),
+              "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+              "decode_tokens_per_s": round(world * w.batch / (ms * 1e-3), 1),
+              "roofline": {"bound": "hbm", "achieved": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                           "unit": "GB/s", "frac": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                           "kernel": "paged_decode_kernel<bf16, e4m3>", "alg_bytes_per_launch": dec_bytes,
+                           "ms_per_launch": round(dec_ms, 5)},
+              "gpu_launches": 2 * L * args.steps}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return result
+
+
+def bench_verify(args, device, q_len=4):
+    """Speculative-decoding verify pass (q_len query tokens per sequence), one layer of the batch-256 workload."""
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b256_28l(num_layers=1)
+    t = wl.verify_tensors(w, q_len, device)
+    meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+    ws = pkv.decode_workspace(w.batch, q_len * w.num_q_heads, w.head_dim, 0, device=device)
+    out = torch.empty_like(t["q"])
+    flush = torch.empty(torch.cuda.get_device_properties(device).L2_cache_size // 2, dtype=torch.float32,
+                        device=device)
+    times = []
+    for i in range(args.warmup + max(10, args.steps)):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.paged_verify_attn(t["q"], t["k_cache"], t["v_cache"], meta["block_tables"], meta["context_lens"],
+                              w.scale, workspace=ws, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    assert pkv.device_error() == 0
+    ms = statistics.median(times)
+    nbytes = (sum(w.context_lens) * w.num_kv_heads * w.head_dim * 2 * 2 + 2 * w.batch * q_len * w.num_q_heads *
+              w.head_dim * 2 + sum(-(-n // w.block_size) for n in w.context_lens) * 4 + 4 * w.batch)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = measured_peaks()[0]
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": w.name.replace("28layers", "1layer") + f"-verify-q{q_len}", "q_len": q_len,
+            "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
+            "tokens_per_s": round(w.batch * q_len / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+
+
 def flush_l2(buf):
     buf.add_(1)
 
@@ -491,6 +607,10 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, res["st"])
+    res["st"] = None
+    torch.cuda.empty_cache()
+    line["fp8_kv"] = bench_fp8(args, device, world)
+    line["verify"] = bench_verify(args, device)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

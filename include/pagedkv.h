@@ -183,6 +183,42 @@ int pkv_paged_verify_attn(void* out, const void* q, const void* k_cache, const v
                           pkv_stream_t stream);
 
 /*
+ * FP8 KV cache.  The pages name a reduced-precision cache ("10 Serving
+ * Engines", 10.2.2, --kv-cache-dtype) without a format; this library stores
+ * OCP FP8 E4M3 with one float scale for K and one for V (per layer): an
+ * element x is stored as e4m3(x / scale), rounded to nearest even and
+ * saturated to +-448, and read back as value(code) * scale.  The cache layout
+ * is the bf16 one with one byte per element.
+ *
+ * kv_store_fp8: pkv_kv_store's slot scatter, quantizing bf16 rows.
+ *   k, v            device, bf16 [num_tokens, num_kv_heads, head_dim]
+ *   k_cache, v_cache device, E4M3 bytes [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scale, v_scale finite and > 0
+ * The division x / scale is an IEEE float32 division, so the stored codes are
+ * exactly determined.  num_kv_heads * head_dim must be a multiple of 16.
+ */
+int pkv_kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                     const int32_t* slot_mapping, int32_t num_tokens, int32_t num_blocks,
+                     int32_t block_size, int32_t num_kv_heads, int32_t head_dim, float k_scale,
+                     float v_scale, pkv_stream_t stream);
+
+/*
+ * paged_decode_attn over an FP8 E4M3 cache: the same result as
+ * pkv_paged_decode_attn on the dequantized cache (value(code) * scale).
+ *   q, out          device, bf16 [batch, num_q_heads, head_dim]
+ *   k_cache,v_cache device, E4M3 bytes, layout as above
+ *   workspace       as for pkv_paged_decode_attn (same size function)
+ * Supported: head_dim 128; G in {1, 2, 4}; num_kv_heads in [1, 8].
+ */
+int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks, float scale, float k_scale, float v_scale,
+                              int32_t num_splits, void* workspace, size_t workspace_bytes,
+                              pkv_stream_t stream);
+
+/*
  * paged_decode_attn without a caller-provided workspace (no counterpart in the
  * pages: it is an addition of this library).
  *

@@ -11,10 +11,12 @@ from .ops import (  # noqa: F401
     decode_workspace_bytes,
     device_error,
     kv_store,
+    kv_store_fp8,
     paged_decode_attn,
+    paged_decode_attn_fp8,
     paged_varlen_prefill_attn,
     paged_verify_attn,
 )
 
-__all__ = ["kv_store", "paged_decode_attn", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
+__all__ = ["kv_store", "kv_store_fp8", "paged_decode_attn", "paged_decode_attn_fp8", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
            "decode_workspace_bytes", "device_error", "metadata", "ops", "workloads"]

@@ -87,6 +87,7 @@ extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cac
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.v_scale = 1.f;
   p.num_splits = num_splits;
   const int group = num_q_heads / num_kv_heads;
   if (dtype == PKV_BF16) {

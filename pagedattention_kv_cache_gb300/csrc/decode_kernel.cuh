@@ -36,6 +36,7 @@
 
 #include <cfloat>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -61,7 +62,9 @@ struct Shape {
   static constexpr int CPL = CHUNKS / LPT;                  // chunks per lane
   static constexpr int EPL = CPL * EPC;                     // elements per lane
   static constexpr int TPW = 32 / LPT;                      // tokens per warp round
-  static constexpr int ROUNDS = (ROW_BYTES >= 512 || R >= 5) ? 2 : 4;  // rounds per stage per warp
+  // rounds per stage per warp: short rows (FP8, or bf16 with head_dim 64) take
+  // more tokens per stage so a stage still moves a useful number of bytes
+  static constexpr int ROUNDS = (ROW_BYTES >= 512 || R >= 5) ? 2 : ((ROW_BYTES <= 128 && R <= 2) ? 8 : 4);
   static_assert(CPL >= 1, "head row too short for the lane split");
 };
 
@@ -83,7 +86,8 @@ struct Params {
   int hkv;
   int block_size;
   int num_blocks;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (times the K scale for an FP8 cache)
+  float v_scale;     // V scale of an FP8 cache (1 otherwise)
   int num_splits;    // 0 = automatic
   int nw;            // consumer warps
   int wph;           // consumer warps per KV head
@@ -235,10 +239,12 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
 
 // G query heads per KV head, QL query tokens per sequence.  A consumer warp
 // holds R = G * QL rows: row rho is query token rho / G, head g * G + rho % G.
-template <typename T, int D, int G, int QL>
+// T is the q / out element type, TC the cache's (T, or FP8 E4M3 with scales).
+template <typename T, typename TC, int D, int G, int QL>
 __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
   constexpr int R = G * QL;
-  using S = Shape<T, D, R>;
+  using S = Shape<TC, D, R>;
+  constexpr int NQ = S::EPC / Chunk<T>::N;  // q / out chunks per cache chunk
   const int rows_per_seq = QL * p.hq;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -333,10 +339,12 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
       const T* qh =
           static_cast<const T*>(p.q) + ((static_cast<size_t>(seg.b) * QL + h / G) * p.hq + g * G + h % G) * D;
 #pragma unroll
-      for (int k = 0; k < S::CPL; ++k) {
-        const uint4 c = __ldg(reinterpret_cast<const uint4*>(qh) + lig + S::LPT * k);
-        Chunk<T>::unpack(c, &qr[h][k * S::EPC]);
-      }
+      for (int k = 0; k < S::CPL; ++k)
+#pragma unroll
+        for (int u = 0; u < NQ; ++u) {
+          const uint4 c = __ldg(reinterpret_cast<const uint4*>(qh) + (lig + S::LPT * k) * NQ + u);
+          Chunk<T>::unpack(c, &qr[h][k * S::EPC + u * Chunk<T>::N]);
+        }
 #pragma unroll
       for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
     }
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
             float f[S::EPC];
-            Chunk<T>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
 #pragma unroll
             for (int h = 0; h < R; ++h)
 #pragma unroll
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
             float f[S::EPC];
-            Chunk<T>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
 #pragma unroll
             for (int h = 0; h < R; ++h)
 #pragma unroll
@@ -435,6 +443,14 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
       }
       __syncwarp();
       if (lane == 0) pkv::mbar_arrive(&empty[s]);
+    }
+
+    // V's scale is linear in the output: apply it once to the accumulators
+    if constexpr (!std::is_same<TC, T>::value) {
+#pragma unroll
+      for (int h = 0; h < R; ++h)
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) acc[h][e] *= p.v_scale;
     }
 
     // reduce the token groups of the warp (m is already warp-uniform)
@@ -506,7 +522,9 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
             float f[S::EPC];
 #pragma unroll
             for (int e = 0; e < S::EPC; ++e) f[e] = acc[h][k * S::EPC + e] * inv;
-            reinterpret_cast<uint4*>(o)[lig + S::LPT * k] = Chunk<T>::pack(f);
+#pragma unroll
+            for (int u = 0; u < NQ; ++u)
+              reinterpret_cast<uint4*>(o)[(lig + S::LPT * k) * NQ + u] = Chunk<T>::pack(f + u * Chunk<T>::N);
           }
         } else {
           float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
@@ -600,16 +618,16 @@ size_t workspace_layout(int batch, int hq, int d, int num_splits, int sms, size_
   return *off_ml + align256(slots * hq * 2 * sizeof(float));
 }
 
-template <typename T, int D, int G, int QL>
+template <typename T, typename TC, int D, int G, int QL>
 int launch(Params& p, int sms, cudaStream_t stream) {
-  const LaunchShape ls = launch_shape<T, D, G * QL>(p.hkv);
+  const LaunchShape ls = launch_shape<TC, D, G * QL>(p.hkv);
   if (ls.stages < 2) return PKV_EUNSUPPORTED;
   p.nw = ls.nw;
   p.wph = ls.wph;
   p.t_stage = ls.t_stage;
   p.stages = ls.stages;
   p.stage_bytes = ls.stage_bytes;
-  auto kernel = paged_decode_kernel<T, D, G, QL>;
+  auto kernel = paged_decode_kernel<T, TC, D, G, QL>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ls.smem)) !=
       cudaSuccess)
     return PKV_ECUDA;
@@ -626,10 +644,10 @@ int launch(Params& p, int sms, cudaStream_t stream) {
 template <typename T, int D>
 int dispatch_g(Params& p, int group, int sms, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch<T, D, 1, 1>(p, sms, stream);
-    case 2: return launch<T, D, 2, 1>(p, sms, stream);
-    case 4: return launch<T, D, 4, 1>(p, sms, stream);
-    case 8: return launch<T, D, 8, 1>(p, sms, stream);
+    case 1: return launch<T, T, D, 1, 1>(p, sms, stream);
+    case 2: return launch<T, T, D, 2, 1>(p, sms, stream);
+    case 4: return launch<T, T, D, 4, 1>(p, sms, stream);
+    case 8: return launch<T, T, D, 8, 1>(p, sms, stream);
     default: return PKV_EUNSUPPORTED;
   }
 }

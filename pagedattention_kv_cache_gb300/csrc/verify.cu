@@ -15,14 +15,14 @@ template <int G>
 int dispatch_ql(Params& p, int ql, int sms, cudaStream_t stream) {
   using T = __nv_bfloat16;
   switch (ql) {
-    case 1: return launch<T, 128, G, 1>(p, sms, stream);
-    case 2: if constexpr (G * 2 <= 8) return launch<T, 128, G, 2>(p, sms, stream); break;
-    case 3: if constexpr (G * 3 <= 8) return launch<T, 128, G, 3>(p, sms, stream); break;
-    case 4: if constexpr (G * 4 <= 8) return launch<T, 128, G, 4>(p, sms, stream); break;
-    case 5: if constexpr (G * 5 <= 8) return launch<T, 128, G, 5>(p, sms, stream); break;
-    case 6: if constexpr (G * 6 <= 8) return launch<T, 128, G, 6>(p, sms, stream); break;
-    case 7: if constexpr (G * 7 <= 8) return launch<T, 128, G, 7>(p, sms, stream); break;
-    case 8: if constexpr (G * 8 <= 8) return launch<T, 128, G, 8>(p, sms, stream); break;
+    case 1: return launch<T, T, 128, G, 1>(p, sms, stream);
+    case 2: if constexpr (G * 2 <= 8) return launch<T, T, 128, G, 2>(p, sms, stream); break;
+    case 3: if constexpr (G * 3 <= 8) return launch<T, T, 128, G, 3>(p, sms, stream); break;
+    case 4: if constexpr (G * 4 <= 8) return launch<T, T, 128, G, 4>(p, sms, stream); break;
+    case 5: if constexpr (G * 5 <= 8) return launch<T, T, 128, G, 5>(p, sms, stream); break;
+    case 6: if constexpr (G * 6 <= 8) return launch<T, T, 128, G, 6>(p, sms, stream); break;
+    case 7: if constexpr (G * 7 <= 8) return launch<T, T, 128, G, 7>(p, sms, stream); break;
+    case 8: if constexpr (G * 8 <= 8) return launch<T, T, 128, G, 8>(p, sms, stream); break;
     default: break;
   }
   return PKV_EUNSUPPORTED;
@@ -83,6 +83,7 @@ extern "C" int pkv_paged_verify_attn(void* out, const void* q, const void* k_cac
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.v_scale = 1.f;
   p.num_splits = num_splits;
   switch (group) {
     case 1: return dispatch_ql<1>(p, q_len, info.sms, stream);

@@ -63,6 +63,60 @@ def kv_store(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     _lib.check("pkv_kv_store", st)
 
 
+def kv_store_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 slot_mapping: torch.Tensor, k_scale: float, v_scale: float, stream=None) -> None:
+    """Quantizing store: bf16 rows [N, Hkv, D] into E4M3 caches [blocks, bs, Hkv, D] (uint8 or
+    float8_e4m3fn tensors) as e4m3(x / scale); slot -1 skips."""
+    _need(k, "k", dtype=torch.bfloat16, ndim=3)
+    _need(v, "v", dtype=torch.bfloat16, ndim=3)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, ndim=4)
+        if t.element_size() != 1:
+            raise TypeError(f"{name} must be a one-byte (E4M3) tensor")
+    _need(slot_mapping, "slot_mapping", dtype=torch.int32, ndim=1)
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or k_cache.shape[2:] != k.shape[1:]:
+        raise ValueError("expected k, v [N, Hkv, D] and caches [blocks, bs, Hkv, D]")
+    if slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError("slot_mapping length differs from the number of rows")
+    nb, bs, hkv, d = k_cache.shape
+    st = _lib.load().pkv_kv_store_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                                      k.shape[0], nb, bs, hkv, d, ctypes.c_float(k_scale),
+                                      ctypes.c_float(v_scale), _stream(stream))
+    _lib.check("pkv_kv_store_fp8", st)
+
+
+def paged_decode_attn_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                          k_scale: float, v_scale: float, *, num_splits: int = 0,
+                          workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """Decode attention over an E4M3 cache with per-tensor scales; q / out bf16 [B, Hq, D]."""
+    _need(q, "q", dtype=torch.bfloat16, ndim=3)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, ndim=4)
+        if t.element_size() != 1:
+            raise TypeError(f"{name} must be a one-byte (E4M3) tensor")
+    _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    _need(context_lens, "context_lens", dtype=torch.int32, ndim=1)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes between q, caches, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=torch.bfloat16)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, d, num_splits, device=q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().pkv_paged_decode_attn_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), B, hq, hkv, d, bs, nb, ctypes.c_float(scale), ctypes.c_float(k_scale),
+        ctypes.c_float(v_scale), num_splits, ws_ptr, ws_bytes, _stream(stream))
+    _lib.check("pkv_paged_decode_attn_fp8", st)
+    return out
+
+
 def decode_workspace_bytes(batch: int, num_q_heads: int, head_dim: int, num_splits: int = 0) -> int:
     """Bytes of split workspace paged_decode_attn needs on the current device."""
     return int(_lib.load().pkv_paged_decode_workspace_bytes(batch, num_q_heads, head_dim, num_splits))

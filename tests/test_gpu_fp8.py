@@ -1,0 +1,85 @@
+"""GPU parity of the FP8 (E4M3) KV cache: the quantizing store is bit-exact
+against the oracle's codec, and decode over the one-byte cache matches the
+oracle's attention over the dequantized cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_kv_cache_gb300 as pkv
+from pagedattention_kv_cache_gb300 import _lib
+from pagedattention_kv_cache_gb300 import metadata as md
+from pagedattention_kv_cache_gb300 import workloads as wl
+from oracle import attention as oa
+from oracle import fp8 as of8
+from oracle import metadata as om
+
+from _harness import as_np, assert_close
+
+pytestmark = pytest.mark.gpu
+
+K_SCALE, V_SCALE = 1.0 / 64, 3.0 / 256
+
+
+def test_kv_store_fp8_bit_exact_with_saturation():
+    gen = torch.Generator().manual_seed(0)
+    N, nb, bs, hkv, d = 50, 12, 8, 2, 128
+    k = (torch.randn(N, hkv, d, generator=gen) * 3).to(torch.bfloat16)
+    v = (torch.randn(N, hkv, d, generator=gen) * 3).to(torch.bfloat16)
+    k[0, 0, :4] = torch.tensor([1e6, -1e6, 448 * K_SCALE * 1.02, 0.0])  # saturation and zero
+    kc = torch.randint(0, 256, (nb, bs, hkv, d), generator=gen, dtype=torch.uint8)
+    vc = torch.randint(0, 256, (nb, bs, hkv, d), generator=gen, dtype=torch.uint8)
+    slots = torch.randperm(nb * bs, generator=gen)[:N].int()
+    slots[3] = -1
+    gk, gv = kc.cuda(), vc.cuda()
+    pkv.kv_store_fp8(k.cuda(), v.cuda(), gk, gv, slots.cuda(), K_SCALE, V_SCALE)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    wk, wv = of8.kv_store_fp8(kc.numpy(), vc.numpy(), as_np(k), as_np(v), slots.numpy(), K_SCALE, V_SCALE)
+    assert np.array_equal(gk.cpu().numpy(), wk)
+    assert np.array_equal(gv.cpu().numpy(), wv)
+
+
+def _quantized_pool(shape, gen, scale):
+    x = torch.randn(shape, generator=gen).to(torch.bfloat16)
+    return torch.from_numpy(of8.quantize(as_np(x), scale))
+
+
+@pytest.mark.parametrize("group", [1, 2, 4])
+@pytest.mark.parametrize("splits", [0, 1, 5])
+def test_fp8_decode_matches_oracle_on_dequantized_cache(group, splits):
+    w = wl.random_decode(60 + group, batch=12, max_ctx=1200, min_ctx=0, block_size=16, num_q_heads=4 * group,
+                         num_kv_heads=4, head_dim=128, dtype=torch.bfloat16)
+    gen = torch.Generator().manual_seed(group)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc, vc = _quantized_pool(shape, gen, K_SCALE), _quantized_pool(shape, gen, V_SCALE)
+    q = torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+    kn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+    vn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+    meta = md.decode_metadata(w.block_tables, w.context_lens, w.block_size)
+    gm = md.to_device(meta, "cuda")
+    gk, gv = kc.cuda(), vc.cuda()
+    pkv.kv_store_fp8(kn.cuda(), vn.cuda(), gk, gv, gm["slot_mapping"], K_SCALE, V_SCALE)
+    out = pkv.paged_decode_attn_fp8(q.cuda(), gk, gv, gm["block_tables"], gm["context_lens"], w.scale, K_SCALE,
+                                    V_SCALE, num_splits=splits)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    om_ = om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(w.block_tables, w.context_lens)],
+                            w.block_size)
+    wk, wv = of8.kv_store_fp8(kc.numpy(), vc.numpy(), as_np(kn), as_np(vn), om_["slot_mapping"], K_SCALE, V_SCALE)
+    assert np.array_equal(gk.cpu().numpy(), wk) and np.array_equal(gv.cpu().numpy(), wv)
+    ref = oa.paged_decode_attention(as_np(q), of8.dequantize(wk, K_SCALE), of8.dequantize(wv, V_SCALE),
+                                    om_["block_tables"], om_["context_lens"], w.scale)
+    assert_close(out, ref, torch.bfloat16, f"fp8 decode G={group} splits={splits}")
+
+
+def test_fp8_argument_errors():
+    q = torch.zeros(1, 2, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(2, 16, 1, 128, dtype=torch.uint8, device="cuda")
+    bt = torch.zeros(1, 1, dtype=torch.int32, device="cuda")
+    cl = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.PagedKVError):
+        pkv.paged_decode_attn_fp8(q, kc, kc, bt, cl, 0.1, 0.0, 1.0)  # scale must be > 0
+    with pytest.raises(_lib.PagedKVError):
+        pkv.paged_decode_attn_fp8(torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda"), kc, kc, bt, cl, 0.1,
+                                  1.0, 1.0)  # G = 8 is not built for FP8
