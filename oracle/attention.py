@@ -208,3 +208,19 @@ def paged_prefill_attention(q, cu_seqlens_q, cu_seqlens_k, scale: float, *, k_ca
             g = h // group
             out[q0:q1, h] = softmax_attention_rows(q[q0:q1, h], keys[:, g], values[:, g], scale, visible)
     return out
+
+
+def copy_blocks(caches, pairs):
+    """Copy-on-write block copy: for every (src, dst) pair, block dst of every cache
+    becomes a copy of block src; returns updated copies.
+
+    "Warmup Guide -- Inference Serving Internals", chapter 4: a sequence about
+    to write into a block it shares copies that one block first and writes
+    into its private copy.  caches: list of [num_blocks, ...] arrays (K and V
+    of every layer); pairs: [n, 2] with no destination also used as a source.
+    """
+    out = [np.array(c, copy=True) for c in caches]
+    for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
+        for c, orig in zip(out, caches):
+            c[dst] = orig[src]
+    return out

@@ -348,3 +348,22 @@ def test_kv_store_rejects_out_of_pool_slot():
     kc = np.zeros((2, 4, 1, 8))
     with pytest.raises(IndexError):
         oa.kv_store(kc, kc, np.zeros((1, 1, 8)), np.zeros((1, 1, 8)), np.array([8]))
+
+
+def test_copy_blocks_closed_form_and_sharing():
+    rng = np.random.default_rng(60)
+    k = rng.integers(0, 255, size=(6, 4, 2, 8), dtype=np.uint8)
+    v = rng.integers(0, 255, size=(6, 4, 2, 8), dtype=np.uint8)
+    k2, v2 = oa.copy_blocks([k, v], [[1, 4], [2, 5]])
+    np.testing.assert_array_equal(k2[4], k[1])
+    np.testing.assert_array_equal(v2[5], v[2])
+    np.testing.assert_array_equal(k2[[0, 1, 2, 3]], k[[0, 1, 2, 3]])
+    # a sequence that shares a prefix block and then copies it reads the same history
+    kc, vc, bt, ks, vs = _place(rng, [10], 4, 1, 8)
+    q = rng.standard_normal((1, 2, 8))
+    base = oa.paged_decode_attention(q, kc, vc, bt, np.array([10]), 0.5)
+    free = kc.shape[0] - 1
+    kc2, vc2 = oa.copy_blocks([kc, vc], [[bt[0, 1], free]])
+    bt2 = bt.copy()
+    bt2[0, 1] = free
+    np.testing.assert_array_equal(oa.paged_decode_attention(q, kc2, vc2, bt2, np.array([10]), 0.5), base)
