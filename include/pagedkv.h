@@ -183,6 +183,27 @@ int pkv_paged_verify_attn(void* out, const void* q, const void* k_cache, const v
                           pkv_stream_t stream);
 
 /*
+ * copy_blocks: the copy of copy-on-write prefix sharing ("Warmup Guide --
+ * Inference Serving Internals", chapter 4: a sequence about to write into a
+ * block it shares copies that block first and writes into the copy).  For
+ * every pair (src, dst) of block_pairs and every layer l, block dst of
+ * k_caches[l] and of v_caches[l] becomes a byte copy of block src.
+ *
+ *   k_caches, v_caches HOST arrays of num_layers device pointers (<= 128 layers),
+ *                   each a pool of num_blocks blocks of block_bytes bytes
+ *                   (block_size * num_kv_heads * head_dim * element size)
+ *   block_pairs     device, int32 [num_pairs, 2]: (src, dst); a pair with an id
+ *                   outside [0, num_blocks) is skipped and raises
+ *                   PKV_DERR_BLOCK_RANGE; src == dst copies nothing
+ *   block_bytes     multiple of 16
+ * A destination that is also a source in the same call, or two pairs with the
+ * same destination, is a caller error (the result is unspecified).
+ */
+int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                    const int32_t* block_pairs, int32_t num_pairs, int32_t num_blocks,
+                    int64_t block_bytes, pkv_stream_t stream);
+
+/*
  * FP8 KV cache.  The pages name a reduced-precision cache ("10 Serving
  * Engines", 10.2.2, --kv-cache-dtype) without a format; this library stores
  * OCP FP8 E4M3 with one float scale for K and one for V (per layer): an

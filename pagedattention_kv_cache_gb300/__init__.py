@@ -7,6 +7,7 @@ they consume; ``workloads`` draws seeded synthetic inputs.
 
 from . import metadata, ops, workloads  # noqa: F401
 from .ops import (  # noqa: F401
+    copy_blocks,
     decode_workspace,
     decode_workspace_bytes,
     device_error,
@@ -18,5 +19,5 @@ from .ops import (  # noqa: F401
     paged_verify_attn,
 )
 
-__all__ = ["kv_store", "kv_store_fp8", "paged_decode_attn", "paged_decode_attn_fp8", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
+__all__ = ["copy_blocks", "kv_store", "kv_store_fp8", "paged_decode_attn", "paged_decode_attn_fp8", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
            "decode_workspace_bytes", "device_error", "metadata", "ops", "workloads"]

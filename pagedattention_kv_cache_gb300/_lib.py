@@ -45,6 +45,8 @@ SIGNATURES = [
     ("pkv_paged_decode_workspace_bytes", _S, [_I, _I, _I, _I]),
     ("pkv_paged_decode_attn", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, ctypes.c_int, _P]),
+    ("pkv_copy_blocks", ctypes.c_int,
+     [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), _I, _P, _I, _I, ctypes.c_int64, _P]),
     ("pkv_kv_store_fp8", ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P]),
     ("pkv_paged_decode_attn_fp8", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I, _P, _S, _P]),

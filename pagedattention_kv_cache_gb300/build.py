@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedkv.so")
-SOURCES = ["api.cu", "kv_store.cu", "decode.cu", "verify.cu", "fp8.cu", "prefill.cu", "prefill_tc.cu"]
+SOURCES = ["api.cu", "kv_store.cu", "decode.cu", "verify.cu", "fp8.cu", "blocks.cu", "prefill.cu", "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{os.path.join(ROOT, 'include')}"]

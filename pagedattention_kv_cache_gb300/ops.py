@@ -63,6 +63,29 @@ def kv_store(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     _lib.check("pkv_kv_store", st)
 
 
+def copy_blocks(k_caches: list[torch.Tensor], v_caches: list[torch.Tensor], block_pairs: torch.Tensor,
+                stream=None) -> None:
+    """Copy-on-write block copies: for each (src, dst) row of block_pairs (int32 [n, 2]),
+    block dst of every layer's K and V pool becomes a copy of block src."""
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("need one K and one V pool per layer")
+    shape = k_caches[0].shape
+    for t in list(k_caches) + list(v_caches):
+        _need(t, "cache")
+        if t.shape != shape or t.dtype != k_caches[0].dtype:
+            raise ValueError("every pool must have the same shape and dtype")
+    _need(block_pairs, "block_pairs", dtype=torch.int32, ndim=2)
+    if block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be [n, 2]")
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_caches])
+    vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
+    block_bytes = k_caches[0][0].numel() * k_caches[0].element_size()
+    st = _lib.load().pkv_copy_blocks(kp, vp, L, _ptr(block_pairs), block_pairs.shape[0], shape[0], block_bytes,
+                                     _stream(stream))
+    _lib.check("pkv_copy_blocks", st)
+
+
 def kv_store_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  slot_mapping: torch.Tensor, k_scale: float, v_scale: float, stream=None) -> None:
     """Quantizing store: bf16 rows [N, Hkv, D] into E4M3 caches [blocks, bs, Hkv, D] (uint8 or
