@@ -50,6 +50,19 @@ constexpr int kWorkspaceCtasPerSm = 2;  // workspace sized for up to this many C
 constexpr int kMaxStages = 4;
 constexpr int kSmemBudget = 200 * 1024;
 
+// d0,d1 += (a0,a1) * (b0,b1) as one packed f32x2 fma (sm_100 family): half
+// the issue slots of two scalar fmas, same rounding per lane.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "fma.rn.f32x2 d, a, b, d;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Register shape of a consumer warp that holds R query rows (query heads x
 // query tokens) of one KV head.
 template <typename T, int D, int R>
@@ -376,6 +389,10 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
         for (int h = 0; h < R; ++h) dot[h] = 0.f;
         if (valid) {
           const unsigned char* row = ks + (static_cast<size_t>(tt) * p.hkv + g) * S::ROW_BYTES;
+          // even and odd elements accumulate in the two lanes of an f32x2 pair
+          float odd[R];
+#pragma unroll
+          for (int h = 0; h < R; ++h) odd[h] = 0.f;
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
             float f[S::EPC];
@@ -383,8 +400,11 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
 #pragma unroll
             for (int h = 0; h < R; ++h)
 #pragma unroll
-              for (int e = 0; e < S::EPC; ++e) dot[h] = fmaf(qr[h][k * S::EPC + e], f[e], dot[h]);
+              for (int e = 0; e < S::EPC; e += 2)
+                fma2(dot[h], odd[h], qr[h][k * S::EPC + e], qr[h][k * S::EPC + e + 1], f[e], f[e + 1]);
           }
+#pragma unroll
+          for (int h = 0; h < R; ++h) dot[h] += odd[h];
         }
 #pragma unroll
         for (int h = 0; h < R; ++h) {
@@ -437,7 +457,8 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
 #pragma unroll
             for (int h = 0; h < R; ++h)
 #pragma unroll
-              for (int e = 0; e < S::EPC; ++e) acc[h][k * S::EPC + e] = fmaf(sc[r][h], f[e], acc[h][k * S::EPC + e]);
+              for (int e = 0; e < S::EPC; e += 2)
+                fma2(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], sc[r][h], sc[r][h], f[e], f[e + 1]);
           }
         }
       }
