@@ -250,6 +250,77 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
   return true;
 }
 
+// Called by all consumer threads after this CTA wrote its part of a split
+// sequence: the part that arrives last (atomic ticket, nothing waits) merges
+// every part's (o, m, l) by log-sum-exp and writes the output.  One warp per
+// output row: lanes reduce the row's maximum and denominator over the parts
+// with shuffles, then each lane owns D / 32 columns and sums the parts eight
+// at a time, so a long context split over dozens of CTAs merges in a few
+// round trips to L2.
+template <typename T, int D>
+__device__ __forceinline__ void combine_if_last(const Params& p, const Segment& seg, int rows_per_seq, int* sh_flag,
+                                                int nthreads_c) {
+  const int tid = threadIdx.x;
+  pkv::named_barrier_sync(1, nthreads_c);
+  if (tid == 0) {
+    __threadfence();
+    const int ticket = atomicAdd(p.counters + seg.b, 1);
+    sh_flag[0] = ticket == seg.nparts - 1;
+  }
+  pkv::named_barrier_sync(1, nthreads_c);
+  if (sh_flag[0]) {
+    __threadfence();
+    constexpr int PER = D / 32;
+    const int warp = tid / 32;
+    const int lane = tid % 32;
+    const int np = seg.nparts;
+    T* out = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
+    for (int row = warp; row < rows_per_seq; row += nthreads_c / 32) {
+      const float* ml_row = p.part_ml + (static_cast<size_t>(seg.first_slot) * rows_per_seq + row) * 2;
+      const size_t ml_stride = static_cast<size_t>(rows_per_seq) * 2;
+      float mm = -INFINITY;
+      for (int j = lane; j < np; j += 32) mm = fmaxf(mm, __ldcg(ml_row + j * ml_stride));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+      float ll = 0.f;
+      for (int j = lane; j < np; j += 32) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_row + j * ml_stride));
+        ll += exp2f(v.x - mm) * v.y;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, off);
+      const float inv = 1.f / ll;
+      const float* o_row = p.part_o + (static_cast<size_t>(seg.first_slot) * rows_per_seq + row) * D + lane * PER;
+      const size_t o_stride = static_cast<size_t>(rows_per_seq) * D;
+      float acc[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < np; ++j) {
+        const float w = exp2f(__ldcg(ml_row + j * ml_stride) - mm);
+        float v[PER];
+        if constexpr (PER == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(o_row + j * o_stride));
+          v[0] = x.x;
+          v[1] = x.y;
+          v[2] = x.z;
+          v[3] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(o_row + j * o_stride));
+          v[0] = x.x;
+          v[1] = x.y;
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < PER; ++e) out[static_cast<size_t>(row) * D + lane * PER + e] = static_cast<T>(acc[e] * inv);
+    }
+    if (tid == 0) p.counters[seg.b] = 0;
+  }
+  pkv::named_barrier_sync(1, nthreads_c);
+}
+
 // G query heads per KV head, QL query tokens per sequence.  A consumer warp
 // holds R = G * QL rows: row rho is query token rho / G, head g * G + rho % G.
 // T is the q / out element type, TC the cache's (T, or FP8 E4M3 with scales).
@@ -563,38 +634,317 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
       }
     }
 
-    if (seg.nparts > 1) {
-      // the last part to arrive merges all parts of the sequence
-      pkv::named_barrier_sync(1, nthreads_c);
-      if (tid == 0) {
-        __threadfence();
-        const int ticket = atomicAdd(p.counters + seg.b, 1);
-        sh_flag[0] = ticket == seg.nparts - 1;
+    if (seg.nparts > 1) combine_if_last<T, D>(p, seg, rows_per_seq, sh_flag, nthreads_c);
+    return true;
+  });
+}
+
+// ------------------------------------------------------------------ tensor-core variant
+//
+// With R >= 3 rows per KV head (grouped-query heads x verify tokens) the
+// CUDA-core loop above runs out of registers and issue slots before HBM is
+// saturated.  This variant keeps the same CTA plan, producer, split and
+// combine, but each consumer warp computes its 16-token chunk of a stage with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate): S = Q K^T with the R rows in
+// the M dimension (rows >= R are zero), online softmax on the accumulator
+// fragments (O rescaled only when a row maximum grows by more than 2^8), and
+// O += P V with P taken straight from the S fragments.  Each token's row of
+// all KV heads is copied to shared memory at a stride padded by 16 bytes, so
+// the eight keys an ldmatrix reads sit in eight different bank groups.
+
+constexpr int kMmaTokens = 16;  // keys per consumer warp per stage
+constexpr int kMmaPad = 16;     // bytes after each token row in shared memory
+
+template <int G, int QL>
+__global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p) {
+  using T = __nv_bfloat16;
+  constexpr int D = 128;
+  constexpr int R = G * QL;
+  static_assert(R <= 16, "at most 16 rows per KV head");
+  constexpr float kRescale = 8.0f;
+  const int rows_per_seq = QL * p.hq;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+  const int nw = p.nw;
+  const int ts = p.hkv * D * 2 + kMmaPad;  // shared-memory stride of one token's row
+
+  unsigned char* stage_base = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  long long* sh = reinterpret_cast<long long*>(empty + kMaxStages);
+  int* sh_flag = reinterpret_cast<int*>(sh + 64);
+  float* merge = reinterpret_cast<float*>(sh_flag + 32);
+  volatile int* abort_flag = sh_flag + 1;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      pkv::mbar_init(&full[s], 1);
+      pkv::mbar_init(&empty[s], nw);
+    }
+    pkv::fence_mbar_init();
+  }
+  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+    if (context_len(p, b) != 0) continue;
+    T* o = static_cast<T*>(p.out) + static_cast<size_t>(b) * rows_per_seq * D;
+    for (int i = tid; i < rows_per_seq * D; i += blockDim.x) o[i] = static_cast<T>(0.0f);
+  }
+  Plan plan;
+  if (p.num_splits > 0) {
+    plan_fixed(p, plan);
+    __syncthreads();
+  } else {
+    plan_auto(p, plan, sh);
+  }
+
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t policy = pkv::l2_evict_first_policy();
+    const uint32_t head_row = static_cast<uint32_t>(p.hkv) * D * 2;
+    int it = 0;
+    for_each_segment(p, plan, [&](const Segment& seg) -> bool {
+      const int32_t* table = p.block_tables + static_cast<size_t>(seg.b) * p.max_blocks;
+      for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
+        const int s = it % p.stages;
+        const uint32_t use = it / p.stages;
+        if (use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
+        const int nt = min(p.t_stage, seg.t1 - t);
+        unsigned char* ks = stage_base + s * p.stage_bytes;
+        unsigned char* vs = ks + p.stage_bytes / 2;
+        for (int tt = t; tt < t + nt;) {
+          const int blk = tt / p.block_size;
+          const int off = tt - blk * p.block_size;
+          const int n = min(p.block_size - off, t + nt - tt);
+          const int phys = __ldg(table + blk);
+          if (phys < 0 || phys >= p.num_blocks) {
+            pkv::raise_error(p.err, PKV_DERR_BLOCK_RANGE);
+          } else {
+            pkv::mbar_expect_tx(&full[s], 2 * n * head_row);
+            const size_t src0 = (static_cast<size_t>(phys) * p.block_size + off) * head_row;
+            for (int u = 0; u < n; ++u) {
+              const size_t src = src0 + static_cast<size_t>(u) * head_row;
+              const size_t dst = static_cast<size_t>(tt - t + u) * ts;
+              pkv::bulk_g2s(ks + dst, p.k_cache + src, head_row, &full[s], policy);
+              pkv::bulk_g2s(vs + dst, p.v_cache + src, head_row, &full[s], policy);
+            }
+          }
+          tt += n;
+        }
+        pkv::mbar_arrive(&full[s]);
+      }
+      return true;
+    });
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = warp % p.hkv;
+  const int phase = warp / p.hkv;
+  const int r0 = lane >> 2;  // fragment rows r0 and r0 + 8
+  const int c = lane & 3;
+  const int nthreads_c = nw * 32;
+  const uint32_t stage_addr = pkv::smem_u32(stage_base);
+  int it = 0;
+
+  for_each_segment(p, plan, [&](const Segment& seg) -> bool {
+    // Q as the A operand: rows r0 / r0 + 8, columns 16 kk + 2c (+1) and + 8
+    uint32_t qf[8][4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int rho = r0 + 8 * hh;
+      const uint32_t* qrow =
+          rho < R ? reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) +
+                                                      ((static_cast<size_t>(seg.b) * QL + rho / G) * p.hq + g * G +
+                                                       rho % G) * D)
+                  : nullptr;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qf[kk][hh] = qrow ? __ldg(qrow + kk * 8 + c) : 0u;
+        qf[kk][2 + hh] = qrow ? __ldg(qrow + kk * 8 + 4 + c) : 0u;
+      }
+    }
+    const int lim0 = seg.ctx - QL + (r0 < R ? r0 / G : 0);
+    const int lim1 = seg.ctx - QL + (r0 + 8 < R ? (r0 + 8) / G : 0);
+    float o[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
+
+    for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
+      const int s = it % p.stages;
+      const uint32_t use = it / p.stages;
+      wait_or_abort(&full[s], use & 1u, abort_flag, p.err);
+      const int nt = min(p.t_stage, seg.t1 - t);
+      const int tt0 = phase * kMmaTokens;
+      const int nv = min(max(nt - tt0, 0), kMmaTokens);  // valid keys of this warp's chunk
+      if (nv > 0) {
+        const uint32_t kbase = stage_addr + s * p.stage_bytes + tt0 * ts + g * D * 2;
+        const uint32_t vbase = kbase + p.stage_bytes / 2;
+        if (nv < kMmaTokens) {
+          // V rows past the last key hold stale bytes: zero them so 0 * stale never reaches O
+          unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + tt0 * ts + g * D * 2;
+          for (int idx = lane; idx < (kMmaTokens - nv) * 16; idx += 32)
+            *reinterpret_cast<uint4*>(vrows + (nv + idx / 16) * ts + (idx % 16) * 16) = make_uint4(0, 0, 0, 0);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        // S = Q K^T for 16 keys (two n-tiles of 8)
+        float sacc[2][4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[nb][e] = 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            uint32_t b[4];
+            pkv::ldsm_x4(kbase + (nb * 8 + (lane & 7)) * ts + (k4 * 4 + (lane >> 3)) * 16, b);
+            pkv::mma_bf16_16816(sacc[nb], qf[2 * k4], b[0], b[1]);
+            pkv::mma_bf16_16816(sacc[nb], qf[2 * k4 + 1], b[2], b[3]);
+          }
+        }
+        // scale, mask, online softmax per row (lazy rescale of O)
+        float mt[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = nb * 8 + 2 * c + (e & 1);
+            float x = sacc[nb][e] * p.scale_log2;
+            const bool visible = key < nv && (QL == 1 || t + tt0 + key <= ((e < 2) ? lim0 : lim1));
+            x = visible ? x : -INFINITY;
+            sacc[nb][e] = x;
+            mt[e >> 1] = fmaxf(mt[e >> 1], x);
+          }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 1));
+          mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 2));
+          const float mn = fmaxf(m[hh], mt[hh]);
+          if (mn > m[hh] + kRescale || (m[hh] == -INFINITY && mn != -INFINITY)) {
+            const float corr = exp2f(m[hh] - mn);  // 0 while nothing has been accumulated
+            l[hh] *= corr;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              o[j][2 * hh] *= corr;
+              o[j][2 * hh + 1] *= corr;
+            }
+            m[hh] = mn;
+          }
+        }
+        const float mu0 = m[0] == -INFINITY ? 0.f : m[0];
+        const float mu1 = m[1] == -INFINITY ? 0.f : m[1];
+        uint32_t pf[4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(exp2f(sacc[nb][0] - mu0), exp2f(sacc[nb][1] - mu0));
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(exp2f(sacc[nb][2] - mu1), exp2f(sacc[nb][3] - mu1));
+          l[0] += __low2float(lo) + __high2float(lo);
+          l[1] += __low2float(hi) + __high2float(hi);
+          pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
+          pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        // O += P V over the 16 keys: 16 n-tiles of 8 columns
+#pragma unroll
+        for (int jp = 0; jp < 8; ++jp) {
+          uint32_t b[4];
+          pkv::ldsm_x4_trans(vbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * ts + (2 * jp + (lane >> 4)) * 16, b);
+          pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
+          pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) pkv::mbar_arrive(&empty[s]);
+    }
+
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
+      l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
+    }
+
+    // merge the warps that share KV head g (token phases)
+    if (p.wph > 1) {
+      const int rec = D + 2;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int rho = r0 + 8 * hh;
+        if (rho < R) {
+          float* dstm = merge + (static_cast<size_t>(warp) * R + rho) * rec;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<float2*>(dstm + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
+          if (c == 0) {
+            dstm[D] = m[hh];
+            dstm[D + 1] = l[hh];
+          }
+        }
       }
       pkv::named_barrier_sync(1, nthreads_c);
-      if (sh_flag[0]) {
-        __threadfence();
-        T* o = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
-        for (int i = tid; i < rows_per_seq * D; i += nthreads_c) {
-          const int head = i / D;
-          float mm = -INFINITY;
-          for (int j = 0; j < seg.nparts; ++j)
-            mm = fmaxf(mm, __ldcg(p.part_ml + (static_cast<size_t>(seg.first_slot + j) * rows_per_seq + head) * 2));
-          float ll = 0.f, oo = 0.f;
-          for (int j = 0; j < seg.nparts; ++j) {
-            const size_t slot = seg.first_slot + j;
-            const float2 ml =
-                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * rows_per_seq + head) * 2));
-            const float w = exp2f(ml.x - mm);
-            ll += w * ml.y;
-            oo += w * __ldcg(p.part_o + slot * rows_per_seq * D + i);
+      if (phase == 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rho = r0 + 8 * hh;
+          if (rho >= R) continue;
+          float mm = m[hh];
+          for (int ph = 1; ph < p.wph; ++ph)
+            mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec + D]);
+          const float w0 = mm == -INFINITY ? 0.f : exp2f(m[hh] - mm);
+          float ll = l[hh] * w0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            o[j][2 * hh] *= w0;
+            o[j][2 * hh + 1] *= w0;
           }
-          o[i] = static_cast<T>(oo / ll);
+          for (int ph = 1; ph < p.wph; ++ph) {
+            const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec;
+            const float w = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mm);
+            ll += w * src[D + 1];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 v = *reinterpret_cast<const float2*>(src + j * 8 + 2 * c);
+              o[j][2 * hh] += w * v.x;
+              o[j][2 * hh + 1] += w * v.y;
+            }
+          }
+          m[hh] = mm;
+          l[hh] = ll;
         }
-        if (tid == 0) p.counters[seg.b] = 0;
       }
       pkv::named_barrier_sync(1, nthreads_c);
     }
+
+    // write the result (whole sequence) or this part's state
+    if (phase == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int rho = r0 + 8 * hh;
+        if (rho >= R) continue;
+        const int head = (rho / G) * p.hq + g * G + rho % G;
+        if (seg.nparts == 1) {
+          const float inv = 1.f / l[hh];
+          uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
+                                                       (static_cast<size_t>(seg.b) * rows_per_seq + head) * D);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) orow[j * 4 + c] = pkv::pack_bf16x2(o[j][2 * hh] * inv, o[j][2 * hh + 1] * inv);
+        } else {
+          float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<float2*>(po + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
+          if (c == 0)
+            *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
+                make_float2(m[hh], l[hh]);
+        }
+      }
+    }
+    if (seg.nparts > 1) combine_if_last<T, D>(p, seg, rows_per_seq, sh_flag, nthreads_c);
     return true;
   });
 }
@@ -662,13 +1012,51 @@ int launch(Params& p, int sms, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+template <int G, int QL>
+int launch_mma(Params& p, int sms, cudaStream_t stream) {
+  constexpr int R = G * QL;
+  LaunchShape ls;
+  ls.wph = p.hkv >= 8 ? 1 : 8 / p.hkv;
+  ls.nw = p.hkv * ls.wph;
+  ls.t_stage = kMmaTokens * ls.wph;
+  const size_t ts = static_cast<size_t>(p.hkv) * 128 * 2 + kMmaPad;
+  ls.stage_bytes = static_cast<size_t>(ls.t_stage) * ts * 2;
+  const size_t misc = 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
+                      (ls.wph > 1 ? static_cast<size_t>(ls.nw) * R * (128 + 2) * sizeof(float) : 0);
+  const int stages = static_cast<int>((kSmemBudget - misc) / ls.stage_bytes);
+  ls.stages = stages > kMaxStages ? kMaxStages : stages;
+  if (ls.stages < 2) return PKV_EUNSUPPORTED;
+  ls.smem = ls.stages * ls.stage_bytes + misc;
+  p.nw = ls.nw;
+  p.wph = ls.wph;
+  p.t_stage = ls.t_stage;
+  p.stages = ls.stages;
+  p.stage_bytes = ls.stage_bytes;
+  auto kernel = paged_decode_mma_kernel<G, QL>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ls.smem)) !=
+      cudaSuccess)
+    return PKV_ECUDA;
+  unsigned grid;
+  if (p.num_splits > 0)
+    grid = static_cast<unsigned>(static_cast<long long>(p.batch) * p.num_splits);
+  else
+    grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
+  if (grid == 0) return PKV_OK;
+  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 template <typename T, int D>
 int dispatch_g(Params& p, int group, int sms, cudaStream_t stream) {
   switch (group) {
     case 1: return launch<T, T, D, 1, 1>(p, sms, stream);
     case 2: return launch<T, T, D, 2, 1>(p, sms, stream);
-    case 4: return launch<T, T, D, 4, 1>(p, sms, stream);
-    case 8: return launch<T, T, D, 8, 1>(p, sms, stream);
+    case 4:
+      if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) return launch_mma<4, 1>(p, sms, stream);
+      return launch<T, T, D, 4, 1>(p, sms, stream);
+    case 8:
+      if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) return launch_mma<8, 1>(p, sms, stream);
+      return launch<T, T, D, 8, 1>(p, sms, stream);
     default: return PKV_EUNSUPPORTED;
   }
 }

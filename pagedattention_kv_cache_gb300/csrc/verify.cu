@@ -11,18 +11,25 @@
 
 namespace {
 
+// Rows per KV head R = G * q_len: the CUDA-core kernel for R <= 2, the
+// tensor-core (mma.sync) kernel for 3 <= R <= 16.
+template <int G, int QL>
+int launch_rows(Params& p, int sms, cudaStream_t stream) {
+  if constexpr (G * QL <= 2) return launch<__nv_bfloat16, __nv_bfloat16, 128, G, QL>(p, sms, stream);
+  else return launch_mma<G, QL>(p, sms, stream);
+}
+
 template <int G>
 int dispatch_ql(Params& p, int ql, int sms, cudaStream_t stream) {
-  using T = __nv_bfloat16;
   switch (ql) {
-    case 1: return launch<T, T, 128, G, 1>(p, sms, stream);
-    case 2: if constexpr (G * 2 <= 8) return launch<T, T, 128, G, 2>(p, sms, stream); break;
-    case 3: if constexpr (G * 3 <= 8) return launch<T, T, 128, G, 3>(p, sms, stream); break;
-    case 4: if constexpr (G * 4 <= 8) return launch<T, T, 128, G, 4>(p, sms, stream); break;
-    case 5: if constexpr (G * 5 <= 8) return launch<T, T, 128, G, 5>(p, sms, stream); break;
-    case 6: if constexpr (G * 6 <= 8) return launch<T, T, 128, G, 6>(p, sms, stream); break;
-    case 7: if constexpr (G * 7 <= 8) return launch<T, T, 128, G, 7>(p, sms, stream); break;
-    case 8: if constexpr (G * 8 <= 8) return launch<T, T, 128, G, 8>(p, sms, stream); break;
+    case 1: return launch_rows<G, 1>(p, sms, stream);
+    case 2: if constexpr (G * 2 <= 16) return launch_rows<G, 2>(p, sms, stream); break;
+    case 3: if constexpr (G * 3 <= 16) return launch_rows<G, 3>(p, sms, stream); break;
+    case 4: if constexpr (G * 4 <= 16) return launch_rows<G, 4>(p, sms, stream); break;
+    case 5: if constexpr (G * 5 <= 16) return launch_rows<G, 5>(p, sms, stream); break;
+    case 6: if constexpr (G * 6 <= 16) return launch_rows<G, 6>(p, sms, stream); break;
+    case 7: if constexpr (G * 7 <= 16) return launch_rows<G, 7>(p, sms, stream); break;
+    case 8: if constexpr (G * 8 <= 16) return launch_rows<G, 8>(p, sms, stream); break;
     default: break;
   }
   return PKV_EUNSUPPORTED;
@@ -43,7 +50,8 @@ extern "C" int pkv_paged_verify_attn(void* out, const void* q, const void* k_cac
   if (dtype != PKV_BF16 || head_dim != 128) return PKV_EUNSUPPORTED;
   if (num_kv_heads > 8) return PKV_EUNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
-  if ((group != 1 && group != 2 && group != 4 && group != 8) || group * q_len > 8) return PKV_EUNSUPPORTED;
+  if ((group != 1 && group != 2 && group != 4 && group != 8) || group * q_len > 16 || q_len > 8)
+    return PKV_EUNSUPPORTED;
   if (static_cast<long long>(max_blocks_per_seq) * block_size > INT32_MAX) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_EINVAL;

@@ -48,7 +48,7 @@ def run_verify(w, q_len, num_splits=0):
     return out, g, dm
 
 
-@pytest.mark.parametrize("q_len,group", [(2, 2), (3, 2), (4, 2), (8, 1), (2, 4), (5, 1)])
+@pytest.mark.parametrize("q_len,group", [(2, 2), (3, 2), (4, 2), (8, 1), (2, 4), (5, 1), (8, 2), (4, 4)])
 def test_verify_matches_oracle(q_len, group):
     w = wl.random_decode(40 + q_len, batch=7, max_ctx=700, min_ctx=q_len, block_size=16, num_q_heads=4 * group,
                          num_kv_heads=4, head_dim=128, dtype=torch.bfloat16)
