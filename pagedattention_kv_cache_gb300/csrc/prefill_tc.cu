@@ -19,6 +19,12 @@
 //              row max, exp2, bf16 P written back over its S buffer; O is
 //              rescaled in TMEM only when the row max grows by more than 2^8;
 //              final normalisation and store.
+//   warp 6     V guard: zeroes the V rows past the last key in the last tile,
+//              then hands each V tile to the MMA thread.
+// The MMA thread issues and waits alone: a tcgen05.mma issue blocks until the
+// tensor pipe accepts it, so any instruction between two MMA groups is a
+// bubble in the pipe (a blocking try_wait on an already complete barrier costs
+// about 200 cycles there, which is why the waits below try once first).
 // Two CTAs share an SM (256 TMEM columns and ~98 KB of shared memory each),
 // so one CTA's tensor work and loads overlap the other's softmax.
 // Every wait is bounded; on a timeout the CTA records an error, skips the
@@ -34,7 +40,8 @@ constexpr int kD = 128;
 constexpr int kBM = 128;
 constexpr int kBN = 64;  // keys per tile
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kGuardWarp = 6;
 constexpr int kCtasPerSm = 2;  // two CTAs share an SM: one's MMA and loads hide the other's softmax
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 2 * kBN;  // S buffers at columns 0 and kBN, O (128 columns) after them
@@ -64,7 +71,8 @@ enum Bar {
   P_FULL = 11,
   O_DONE = 13,
   O_FINAL = 14,
-  NUM_BARS = 15
+  V_READY = 15,  // per stage: V loaded and its rows past the last key zeroed
+  NUM_BARS = 17
 };
 
 struct TcParams {
@@ -91,6 +99,8 @@ struct Waiter {
   volatile int* abort_flag;
   unsigned int* err;
   __device__ __forceinline__ void operator()(uint64_t* bar, uint32_t parity) const {
+    // one try_wait first: no shared-memory read of the abort flag on the fast path
+    if (mbar_try_wait(bar, parity)) return;
     if (*abort_flag) return;
     if (!mbar_wait(bar, parity)) {
       *abort_flag = 1;
@@ -115,6 +125,13 @@ __device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, flo
       : "=r"(out)
       : "r"(s0), "r"(s1), "f"(scale), "f"(neg_m));
   return out;
+}
+
+// Maximum of three floats in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // acc (two f32 lanes) += the two bf16 of w, widened exactly.
@@ -175,10 +192,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&bars[V_FULL + s], 1);
       mbar_init(&bars[K_EMPTY + s], 1);
       mbar_init(&bars[V_EMPTY + s], 1);
+      mbar_init(&bars[V_READY + s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[S_FULL + b], 1);
-      mbar_init(&bars[P_FULL + b], 128);
+      mbar_init(&bars[P_FULL + b], 4);  // one arrival per softmax warp
     }
     mbar_init(&bars[O_DONE], 1);
     mbar_init(&bars[O_FINAL], 1);
@@ -191,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
+  // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const Waiter wait{abort_flag, p.err};
 
   if (warp == 0) {
@@ -248,42 +267,60 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp follows the loop and waits every barrier phase in order;
-    // lane 0 issues the tensor-core work.
-    constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
-    constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
-    const uint32_t q_addr = smem_u32(sq);
-    wait(&bars[Q_FULL], 0);
-    auto issue_qk = [&](int j) {
-      const int st = j % kStages;
-      wait(&bars[K_FULL + st], (j / kStages) & 1);
-      if (lane == 0) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
+      // descriptors of the first Q, K and V slabs; later ones differ only in the
+      // start-address field (address >> 4), so they are reached by adding offset >> 4
+      const uint64_t q_desc = tc::smem_desc(smem_u32(sq), 16, 1024);
+      const uint64_t k_desc = tc::smem_desc(smem_u32(sk), 16, 1024);
+      const uint64_t v_desc = tc::smem_desc(smem_u32(sv), kSlabKV, 1024);
+      wait(&bars[Q_FULL], 0);
+      // S(j) = Q K(j)^T into S buffer j & 1
+      auto issue_qk = [&](int j) {
+        const int st = j % kStages;
+        wait(&bars[K_FULL + st], (j / kStages) & 1);
         tc::fence_after_sync();
-        const uint32_t k_addr = smem_u32(sk + st * kTileKV);
-        const uint32_t d = tmem + (j & 1) * kBN;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlabQ + (kk & 3) * 32;
-          const uint64_t a = tc::smem_desc(q_addr + off, 16, 1024);
-          const uint64_t b = tc::smem_desc(k_addr + (kk >> 2) * kSlabKV + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(d, a, b, idesc_qk, kk > 0);
+          const uint32_t a_off = (kk >> 2) * kSlabQ + (kk & 3) * 32;
+          const uint32_t b_off = st * kTileKV + (kk >> 2) * kSlabKV + (kk & 3) * 32;
+          tc::mma_ss(tmem + (j & 1) * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
         }
         tc::commit(&bars[S_FULL + (j & 1)]);
         tc::commit(&bars[K_EMPTY + st]);
+      };
+      issue_qk(0);
+      for (int j = 0; j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) issue_qk(j + 1);  // its S buffer held P(j - 1), consumed already
+        const int st = j % kStages;
+        wait(&bars[V_READY + st], (j / kStages) & 1);
+        wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t b_off = st * kTileKV + kk * 16 * 128;
+          tc::mma_ts(tmem + kColO, tmem + (j & 1) * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&bars[V_EMPTY + st]);
+        tc::commit(&bars[O_DONE]);
       }
-      __syncwarp();
-    };
-    issue_qk(0);
+      tc::commit(&bars[O_FINAL]);
+      // no MMA may be in flight when TMEM is freed
+      wait(&bars[O_FINAL], 0);
+    }
+  } else if (warp == kGuardWarp) {
+    // ------------------------------------------------------------ V guard
+    // Follows every V_FULL phase; in the last tile the V rows past the last key
+    // hold whatever their block had there (or were not loaded): zero them so
+    // 0 * stale never reaches O, then release the tile to the MMA thread.
     for (int j = 0; j < n_tiles; ++j) {
-      if (j + 1 < n_tiles) issue_qk(j + 1);
       const int st = j % kStages;
-      wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
       wait(&bars[V_FULL + st], (j / kStages) & 1);
-      unsigned char* vt = sv + st * kTileKV;
       const int key0 = j * kBN;
       if (key0 + kBN > nk) {
-        // V rows past the last key hold whatever their block had there (or were
-        // not loaded): zero them so 0 * stale never reaches O
+        unsigned char* vt = sv + st * kTileKV;
         const int first = nk - key0;
         for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
           const int rr = first + idx / 16;
@@ -293,23 +330,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       __syncwarp();
-      if (lane == 0) {
-        tc::fence_after_sync();
-        const uint32_t v_addr = smem_u32(vt);
-        const uint32_t pcol = tmem + (j & 1) * kBN;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = tc::smem_desc(v_addr + kk * 16 * 128, kSlabKV, 1024);
-          tc::mma_ts(tmem + kColO, pcol + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::commit(&bars[V_EMPTY + st]);
-        tc::commit(&bars[O_DONE]);
-      }
-      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[V_READY + st]);
     }
-    if (lane == 0) tc::commit(&bars[O_FINAL]);
-    // no MMA may be in flight when TMEM is freed
-    wait(&bars[O_FINAL], 0);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;
@@ -332,56 +354,67 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(lane_addr + b * kBN + c * 32, r + c * 32);
       tc::tmem_wait_ld();
-      const bool need_mask = key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1);
-      // row maximum of the raw scores; the scale (> 0) is applied after
-      float mt = -INFINITY;
-      if (need_mask) {
+      if (key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1)) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < kBN; ++c)
           if (key0 + c > lim) r[c] = __float_as_uint(-INFINITY);
-          mt = fmaxf(mt, __uint_as_float(r[c]));
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, __uint_as_float(r[c]));
       }
+      // row maximum of the raw scores (the scale, > 0, is applied after), as
+      // four independent chains of three-input maxima
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kBN; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mx[u] = max3(mx[u], __uint_as_float(r[c + 2 * u]), __uint_as_float(r[c + 2 * u + 1]));
+      }
+      const float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       const float m_new = fmaxf(m_run, mt * p.scale_log2);
       const bool grow = m_new > m_run + kRescaleLog2 || (m_run == -INFINITY && m_new != -INFINITY);
-      if (__any_sync(0xffffffffu, grow)) {
-        const float factor = (m_run == -INFINITY || m_new <= m_run) ? 1.f : exp2f(m_run - m_new);
-        if (j > 0) {
-          wait(&bars[O_DONE], (j - 1) & 1);
-          tc::fence_after_sync();
-          uint32_t o[32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tc::tmem_ld32(lane_addr + kColO + c * 32, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-            tc::tmem_st32(lane_addr + kColO + c * 32, o);
-          }
-          tc::tmem_wait_st();
-        }
-        l_run *= factor;
+      const bool rescale = __any_sync(0xffffffffu, grow);
+      float factor = 1.f;
+      if (rescale) {
+        factor = (m_run == -INFINITY || m_new <= m_run) ? 1.f : exp2f(m_run - m_new);
         m_run = fmaxf(m_run, m_new);
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       // P = exp2(scale * s - m) rounded to bf16, packed two per column over the
-      // S buffer; the row sum adds the same rounded values (two lanes at a time)
-      uint64_t l_pair = 0;
+      // S buffer; the row sum adds the same rounded values (four accumulators
+      // of two lanes, so the adds do not form one long chain)
+      uint64_t l_pair[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < kBN / 2; ++c) {
         const uint32_t w = exp2_pair_bf16(r[2 * c], r[2 * c + 1], p.scale_log2, -m_use);
-        add_bf16x2(l_pair, w);
+        add_bf16x2(l_pair[c % 4], w);
         r[c] = w;
       }
-      l_run += __uint_as_float(static_cast<uint32_t>(l_pair)) + __uint_as_float(static_cast<uint32_t>(l_pair >> 32));
+      float l_tile = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        l_tile += __uint_as_float(static_cast<uint32_t>(l_pair[u])) +
+                  __uint_as_float(static_cast<uint32_t>(l_pair[u] >> 32));
+      l_run = l_run * factor + l_tile;
 #pragma unroll
       for (int c = 0; c < kBN / 64; ++c) tc::tmem_st32(lane_addr + b * kBN + c * 32, r + c * 32);
+      if (rescale && j > 0) {
+        // O holds the products up to tile j-1: wait for P.V(j-1) (one phase
+        // back at most, see above), then bring O to the new maximum
+        wait(&bars[O_DONE], (j - 1) & 1);
+        tc::fence_after_sync();
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tc::tmem_st32(lane_addr + kColO + c * 32, o);
+        }
+      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&bars[P_FULL + b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[P_FULL + b]);
     }
 
     wait(&bars[O_FINAL], 0);
