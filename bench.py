@@ -162,19 +162,28 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh")
+
+
+def decode_sources_sha256() -> str:
+    """sha256 over the decode kernel's source files, in order."""
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "pagedattention_kv_cache_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def decode_traffic_record():
-    """ncu DRAM bytes per decode launch, valid only for the decode source it was taken on."""
+    """ncu DRAM bytes per decode launch, valid only for the decode sources it was taken on."""
     path = os.path.join(ROOT, "profiles", "paged_decode_qwen3_b256_traffic.md")
-    src = os.path.join(ROOT, "pagedattention_kv_cache_gb300", "csrc", "decode.cu")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m_sha = re.search(r"decode\.cu sha256:\s*([0-9a-f]{64})", text)
+    m_sha = re.search(r"decode sources sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"dram bytes per full launch:\s*([0-9]+)", text)
     if not m_sha or not m_b:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return int(m_b.group(1)) if sha == m_sha.group(1) else None
+    return int(m_b.group(1)) if decode_sources_sha256() == m_sha.group(1) else None
 
 
 # ---------------------------------------------------------------- algorithmic work
