@@ -55,8 +55,9 @@ SIGNATURES = [
     ("pkv_paged_decode_attn_noalloc", ctypes.c_int,
      [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int, _P]),
     ("pkv_paged_varlen_prefill_attn", ctypes.c_int,
-     [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, ctypes.c_int,
-      _P]),
+     [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
+      ctypes.c_int, _P]),
+    ("pkv_paged_varlen_prefill_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
 ]
 
 _lib = None

@@ -339,8 +339,8 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                                              int32_t batch, int32_t total_q, int32_t total_k, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                             int32_t num_blocks, float scale, int32_t causal, pkv_dtype dtype,
-                                             pkv_stream_t stream) {
+                                             int32_t num_blocks, float scale, int32_t causal, void* workspace,
+                                             size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
   if (batch < 0 || total_q < 0 || total_k < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_seqlen_q < 0 || max_seqlen_k < 0)
     return PKV_EINVAL;
@@ -362,6 +362,7 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
     if (!pkv::aligned16(k) || !pkv::aligned16(v)) return PKV_EALIGN;
   }
   if (!pkv::aligned16(out) || !pkv::aligned16(q)) return PKV_EALIGN;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255)) return PKV_EALIGN;
   int st = PKV_OK;
   unsigned int* err = pkv::device_error_word(&st);
   if (st != PKV_OK) return st;
@@ -389,6 +390,8 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
   a.scale = scale;
   a.causal = causal;
   a.group = group;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace ? workspace_bytes : 0;
   if (pkv::prefill_tc_supported(a)) return pkv::prefill_tc_launch(a, stream);
 
   Params p{};
@@ -418,4 +421,10 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
     case 4: return launch<4>(p, max_seqlen_q, stream);
     default: return launch<8>(p, max_seqlen_q, stream);
   }
+}
+
+extern "C" size_t pkv_paged_varlen_prefill_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                                          int32_t head_dim, int32_t max_seqlen_q) {
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim != kD) return 0;
+  return pkv::prefill_tc_workspace_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, max_seqlen_q);
 }

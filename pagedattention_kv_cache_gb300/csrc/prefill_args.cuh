@@ -29,6 +29,8 @@ struct PrefillArgs {
   float scale;
   int causal;
   int group;  // hq / hkv
+  void* workspace;         // split of long items (tcgen05 path), or null
+  size_t workspace_bytes;
 };
 
 // Tensor-core (tcgen05 + TMEM + TMA) path; requires head_dim 128, bf16, and
@@ -36,5 +38,7 @@ struct PrefillArgs {
 // 64 of at least 8.
 bool prefill_tc_supported(const PrefillArgs& a);
 int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
+// Workspace bytes that let the tcgen05 path split long items (0: never splits).
+size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int max_seqlen_q);
 
 }  // namespace pkv

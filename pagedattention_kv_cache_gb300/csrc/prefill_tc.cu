@@ -29,6 +29,8 @@
 // so one CTA's tensor work and loads overlap the other's softmax.
 // Every wait is bounded; on a timeout the CTA records an error, skips the
 // remaining waits and still frees its TMEM.
+#include <algorithm>
+
 #include "prefill_args.cuh"
 #include "tcgen05.cuh"
 
@@ -53,6 +55,18 @@ constexpr uint32_t kBarOffset = kTileQ + 2 * kStages * kTileKV;
 constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
 static_assert(kColO + kD <= kTmemCols, "TMEM plan exceeds the allocation");
 constexpr float kRescaleLog2 = 8.0f;
+
+// Key-range split of long work items, used only when the work items do not
+// fill the GPU (small batches with long histories) and a workspace is given.
+// With P parts chosen on the host, an item with more than kSplitMinTiles key
+// tiles runs as up to P CTAs over consecutive ranges of its key tiles.  Every
+// part but the last to finish publishes its unnormalised O and its row maxima
+// and sums (one record per part); the last merges the records and its own TMEM
+// result by the log-sum-exp rule, in part order, and stores the output.
+constexpr int kSplitMinTiles = 16;
+constexpr int kMaxParts = 8;
+constexpr size_t kRecordBytes = static_cast<size_t>(kBM) * kD * 4 + static_cast<size_t>(kBM) * 8;
+constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the second part's wait for the record
 
 // O_DONE completes once per P.V product; it is waited only one phase behind
 // (lazy rescale).  O_FINAL completes once, after the last P.V: the epilogue and
@@ -93,7 +107,45 @@ struct TcParams {
   int paged;
   int piece_rows;  // rows per K/V TMA box (paged: min(block_size, kBN))
   int q_tiles;
+  int parts_max;        // P: the most parts a long item runs as (1: no split)
+  int* tickets;         // [items]: finish order of a split item's parts, reset by the last
+  int* ready;           // [items]: records published so far, reset by the last
+  unsigned char* records;  // [items][P][kRecordBytes]: O rows (fp32), then m[kBM], l[kBM]
 };
+
+}  // namespace
+
+namespace pkv {
+
+// Parts a long item may run as: enough to give every CTA slot (two per SM)
+// work when the items alone do not, at most kMaxParts; 1 when they do.
+int prefill_tc_parts(int batch, int num_kv_heads, int group, int max_seqlen_q, int sms) {
+  const long long tq = kBM / group;
+  const long long items = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + tq - 1) / tq);
+  const long long slots = static_cast<long long>(sms) * kCtasPerSm;
+  if (items <= 0 || items >= slots) return 1;
+  return static_cast<int>(std::min<long long>(kMaxParts, (slots + items - 1) / items));
+}
+
+// Workspace of the tcgen05 prefill: tickets and ready counts (256-byte aligned
+// blocks), then P records per (sequence, KV head, query tile); 0 when the
+// current device's SMs are filled without splitting.
+size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int max_seqlen_q) {
+  if (batch <= 0 || num_kv_heads <= 0 || max_seqlen_q <= 0) return 0;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return 0;
+  DeviceInfo info;
+  if (device_info(&info) != PKV_OK) return 0;
+  const int parts = prefill_tc_parts(batch, num_kv_heads, group, max_seqlen_q, info.sms);
+  if (parts == 1) return 0;
+  const long long tq = kBM / group;
+  const long long items = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + tq - 1) / tq);
+  const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
+  return 2 * flags + static_cast<size_t>(items) * parts * kRecordBytes;
+}
+
+}  // namespace pkv
+
+namespace {
 
 struct Waiter {
   volatile int* abort_flag;
@@ -151,10 +203,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   constexpr int TQ = kBM / G;
   // blocks launch in linear order: x runs over (sequence, KV head), y over
-  // query tiles from the last (most keys under the causal mask) to the first
+  // query tiles from the last (most keys under the causal mask) to the first,
+  // and, with a workspace, over the two key-range parts of each tile
   const int seq = blockIdx.x / p.hkv;
   const int g = blockIdx.x % p.hkv;
-  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.y);
+  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.y) / p.parts_max;
+  const int part = static_cast<int>(blockIdx.y) % p.parts_max;
   const int q_begin = __ldg(p.cu_q + seq);
   const int nq = __ldg(p.cu_q + seq + 1) - q_begin;
   const int k_begin = __ldg(p.cu_k + seq);
@@ -169,7 +223,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int cached = nk - nq;
   const int tok_last = min(nq, tok0 + TQ) - 1;
   const int keys_needed = p.causal ? cached + tok_last + 1 : nk;
-  const int n_tiles = (keys_needed + kBN - 1) / kBN;
+  const int n_all = (keys_needed + kBN - 1) / kBN;
+  // this CTA's key tiles: j0 .. j0 + n_tiles - 1 (all of them, or one of up to P
+  // consecutive ranges)
+  const int parts = n_all > kSplitMinTiles ? min(p.parts_max, (n_all + kSplitMinTiles - 1) / kSplitMinTiles) : 1;
+  if (part >= parts) return;
+  const int j0 = part * n_all / parts;
+  const int n_tiles = (part + 1) * n_all / parts - j0;
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -179,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_ticket = abort_flag + 1;  // a split item's ticket, broadcast to the softmax warps
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -233,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (use > 0) wait(&bars[(is_v ? V_EMPTY : K_EMPTY) + st], (use - 1) & 1);
         unsigned char* dst = (is_v ? sv : sk) + st * kTileKV;
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-        const int key0 = j * kBN;
+        const int key0 = (j0 + j) * kBN;
         if (p.paged) {
           const uint32_t piece_bytes = p.piece_rows * 128u;
           for (int r = 0; r < kBN; r += p.piece_rows) {
@@ -318,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % kStages;
       wait(&bars[V_FULL + st], (j / kStages) & 1);
-      const int key0 = j * kBN;
+      const int key0 = (j0 + j) * kBN;
       if (key0 + kBN > nk) {
         unsigned char* vt = sv + st * kTileKV;
         const int first = nk - key0;
@@ -348,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
-      const int key0 = j * kBN;
+      const int key0 = (j0 + j) * kBN;
       wait(&bars[S_FULL + b], (j >> 1) & 1);
       tc::fence_after_sync();
 #pragma unroll
@@ -419,21 +480,131 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     wait(&bars[O_FINAL], 0);
     tc::fence_after_sync();
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     __nv_bfloat16* dst =
         p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + head) * kD;
+    if (parts == 1) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      tc::tmem_ld32(lane_addr + kColO + c * 32, o);
-      tc::tmem_wait_ld();
-      if (row_valid) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+        tc::tmem_wait_ld();
+        if (row_valid) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          float f[8];
+          for (int e = 0; e < 32; e += 8) {
+            float f[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
-          reinterpret_cast<uint4*>(dst + c * 32 + e)[0] = Chunk<__nv_bfloat16>::pack(f);
+            for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
+            reinterpret_cast<uint4*>(dst + c * 32 + e)[0] = Chunk<__nv_bfloat16>::pack(f);
+          }
+        }
+      }
+    } else {
+      // Split item: every part but the last to finish publishes O (unnormalised),
+      // m and l of each row; the last waits for those records and merges.
+      const long long item = (static_cast<long long>(seq) * p.hkv + g) * p.q_tiles + qt;
+      auto record = [&](int q) {
+        return reinterpret_cast<float*>(p.records + (static_cast<size_t>(item) * p.parts_max + q) * kRecordBytes);
+      };
+      named_barrier_sync(1, 128);
+      if (threadIdx.x == 64) *s_ticket = atomicAdd(p.tickets + item, 1);
+      named_barrier_sync(1, 128);
+      if (*s_ticket < parts - 1) {
+        float* rec = record(part);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            reinterpret_cast<uint4*>(rec + row * kD + c * 32 + e)[0] = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+        }
+        rec[kBM * kD + row] = m_run;
+        rec[kBM * kD + kBM + row] = l_run;
+        __threadfence();
+        named_barrier_sync(1, 128);
+        if (threadIdx.x == 64) atomicAdd(p.ready + item, 1);
+      } else {
+        if (threadIdx.x == 64) {
+          // the other parts hold their tickets, so they are resident and publish
+          // soon; the wait is still bounded
+          const uint64_t t0 = globaltimer_ns();
+          int ok = 0;
+          while (true) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.ready + item) : "memory");
+            if (v == parts - 1) {
+              ok = 1;
+              break;
+            }
+            if (globaltimer_ns() - t0 > kSplitWaitNs) break;
+            __nanosleep(100);
+          }
+          if (!ok) raise_error(p.err, PKV_DERR_WAIT_TIMEOUT);
+          *s_ticket = ok ? 1 : -1;
+        }
+        named_barrier_sync(1, 128);
+        __threadfence();
+        if (*s_ticket == 1) {
+          // log-sum-exp merge over the parts that saw a key of this row, in part
+          // order, so the result does not depend on the order they finished in
+          float mq[kMaxParts], lq[kMaxParts];
+          float mm = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kMaxParts; ++q) {
+            mq[q] = -INFINITY;
+            lq[q] = 0.f;
+            if (q < parts) {
+              mq[q] = q == part ? m_run : __ldcg(record(q) + kBM * kD + row);
+              lq[q] = q == part ? l_run : __ldcg(record(q) + kBM * kD + kBM + row);
+              if (lq[q] > 0.f) mm = fmaxf(mm, mq[q]);
+            }
+          }
+          float total = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxParts; ++q) {
+            mq[q] = lq[q] > 0.f ? exp2f(mq[q] - mm) : 0.f;  // now the part's weight
+            total += mq[q] * lq[q];
+          }
+          const float inv = total > 0.f ? 1.f / total : 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+            tc::tmem_wait_ld();
+            if (row_valid) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 8) {
+                float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < kMaxParts; ++q) {
+                  if (q >= parts) break;
+                  float v8[8];
+                  if (q == part) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v8[u] = __uint_as_float(o[e + u]);
+                  } else {
+                    const float* src = record(q) + row * kD + c * 32 + e;
+                    const float4 r0 = __ldcg(reinterpret_cast<const float4*>(src));
+                    const float4 r1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                    v8[0] = r0.x, v8[1] = r0.y, v8[2] = r0.z, v8[3] = r0.w;
+                    v8[4] = r1.x, v8[5] = r1.y, v8[6] = r1.z, v8[7] = r1.w;
+                  }
+#pragma unroll
+                  for (int u = 0; u < 8; ++u) f[u] += mq[q] * v8[u];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] *= inv;
+                reinterpret_cast<uint4*>(dst + c * 32 + e)[0] = Chunk<__nv_bfloat16>::pack(f);
+              }
+            }
+          }
+        }
+        named_barrier_sync(1, 128);
+        if (threadIdx.x == 64) {  // leave the item's slots ready for the next call
+          p.tickets[item] = 0;
+          p.ready[item] = 0;
         }
       }
     }
@@ -477,11 +648,24 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   p.paged = paged ? 1 : 0;
   p.piece_rows = piece;
   p.q_tiles = (a.max_seqlen_q + TQ - 1) / TQ;
+  p.parts_max = 1;
+  DeviceInfo info;
+  if (device_info(&info) != PKV_OK) return PKV_ECUDA;
+  const size_t ws_need = prefill_tc_workspace_bytes(a.batch, a.hkv, G, a.max_seqlen_q);
+  if (a.workspace && ws_need > 0 && a.workspace_bytes >= ws_need) {
+    const long long items = static_cast<long long>(a.batch) * a.hkv * p.q_tiles;
+    const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    p.parts_max = prefill_tc_parts(a.batch, a.hkv, G, a.max_seqlen_q, info.sms);
+    p.tickets = reinterpret_cast<int*>(ws);
+    p.ready = reinterpret_cast<int*>(ws + flags);
+    p.records = ws + 2 * flags;
+  }
   auto kernel = prefill_tc_kernel<G>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
       cudaSuccess)
     return PKV_ECUDA;
-  dim3 grid(a.batch * a.hkv, p.q_tiles);
+  dim3 grid(a.batch * a.hkv, p.q_tiles * p.parts_max);
   kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

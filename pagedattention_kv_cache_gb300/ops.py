@@ -242,13 +242,48 @@ def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     return out
 
 
+def prefill_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                            max_seqlen_q: int) -> int:
+    """Bytes of the optional split workspace of paged_varlen_prefill_attn (0: never splits)."""
+    return int(_lib.load().pkv_paged_varlen_prefill_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                                     max_seqlen_q))
+
+
+def prefill_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_seqlen_q: int,
+                      device=None) -> torch.Tensor | None:
+    """A zero-filled workspace (uint8) for paged_varlen_prefill_attn, or None when none is needed."""
+    n = prefill_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seqlen_q)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+_prefill_ws: dict[int, torch.Tensor] = {}
+
+
+def _cached_prefill_workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """One zero-filled workspace per device, grown on demand; the kernel leaves it zeroed."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _prefill_ws.get(idx)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _prefill_ws[idx] = ws
+    return ws
+
+
 def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                               max_seqlen_q: int, max_seqlen_k: int, scale: float, *,
                               k: torch.Tensor | None = None, v: torch.Tensor | None = None,
                               k_cache: torch.Tensor | None = None, v_cache: torch.Tensor | None = None,
                               block_tables: torch.Tensor | None = None, causal: bool = True,
+                              workspace: torch.Tensor | bool | None = None,
                               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Packed varlen prefill attention; keys through block_tables (cache) or from packed k/v."""
+    """Packed varlen prefill attention; keys through block_tables (cache) or from packed k/v.
+
+    workspace: None = a zero-filled workspace cached per device (calls that may
+    overlap on different streams must pass their own); False = never split long
+    query tiles; or a tensor from prefill_workspace().
+    """
     _need(q, "q", ndim=3)
     _need(cu_seqlens_q, "cu_seqlens_q", dtype=torch.int32, ndim=1)
     _need(cu_seqlens_k, "cu_seqlens_k", dtype=torch.int32, ndim=1)
@@ -278,10 +313,20 @@ def paged_varlen_prefill_attn(q: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_se
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", dtype=q.dtype)
+    ws_bytes = 0
+    if workspace is None:
+        ws_bytes = prefill_workspace_bytes(B, hq, hkv, d, int(max_seqlen_q))
+        workspace = _cached_prefill_workspace(ws_bytes, q.device) if ws_bytes > 0 else None
+    elif workspace is False:
+        workspace = None
+    else:
+        _need(workspace, "workspace", dtype=torch.uint8)
+        ws_bytes = workspace.numel()
     st = _lib.load().pkv_paged_varlen_prefill_attn(
         _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), _ptr(block_tables), mb, B, total_q,
-        total_k, hq, hkv, d, bs, nb, ctypes.c_float(scale), 1 if causal else 0, _dtype_code(q), _stream(stream))
+        total_k, hq, hkv, d, bs, nb, ctypes.c_float(scale), 1 if causal else 0, _ptr(workspace), ws_bytes,
+        _dtype_code(q), _stream(stream))
     _lib.check("pkv_paged_varlen_prefill_attn", st)
     return out
 

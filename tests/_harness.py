@@ -89,7 +89,7 @@ def run_decode(w: wl.DecodeWorkload, *, num_splits: int = 0, poison: bool = Fals
 
 
 def run_prefill(w: wl.PrefillWorkload, *, use_tables: bool = True, poison: bool = False, device="cuda",
-                causal: bool = True) -> dict:
+                causal: bool = True, workspace=None) -> dict:
     """Store this round's rows and run varlen prefill on the GPU; compare with the oracle."""
     t = wl.prefill_tensors(w, "cpu", poison=poison)
     meta = md.prefill_metadata(w.block_tables, w.num_cached, w.num_new, w.block_size, always_tables=use_tables)
@@ -99,10 +99,12 @@ def run_prefill(w: wl.PrefillWorkload, *, use_tables: bool = True, poison: bool 
         pkv.kv_store(g["k"], g["v"], g["k_cache"], g["v_cache"], gm["slot_mapping"])
         out = pkv.paged_varlen_prefill_attn(g["q"], gm["cu_seqlens_q"], gm["cu_seqlens_k"], meta["max_seqlen_q"],
                                             meta["max_seqlen_k"], w.scale, k_cache=g["k_cache"],
-                                            v_cache=g["v_cache"], block_tables=gm["block_tables"], causal=causal)
+                                            v_cache=g["v_cache"], block_tables=gm["block_tables"], causal=causal,
+                                            workspace=workspace)
     else:
         out = pkv.paged_varlen_prefill_attn(g["q"], gm["cu_seqlens_q"], gm["cu_seqlens_k"], meta["max_seqlen_q"],
-                                            meta["max_seqlen_k"], w.scale, k=g["k"], v=g["v"], causal=causal)
+                                            meta["max_seqlen_k"], w.scale, k=g["k"], v=g["v"], causal=causal,
+                                            workspace=workspace)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 

@@ -47,6 +47,38 @@ def test_version_and_status_strings():
     assert lib.pkv_status_string(_lib.EWORKSPACE) == b"workspace missing or too small"
 
 
+def test_prefill_workspace_is_zero_when_nothing_splits():
+    # shapes without a tensor-core path, empty batches and (without a GPU) any shape never split
+    _built()
+    lib = _lib.load()
+    assert lib.pkv_paged_varlen_prefill_workspace_bytes(16, 16, 8, 64, 512) == 0  # head_dim 64
+    assert lib.pkv_paged_varlen_prefill_workspace_bytes(16, 48, 8, 128, 512) == 0  # G = 6 unsupported
+    assert lib.pkv_paged_varlen_prefill_workspace_bytes(0, 16, 8, 128, 512) == 0
+    if not torch.cuda.is_available():
+        assert lib.pkv_paged_varlen_prefill_workspace_bytes(1, 16, 8, 128, 512) == 0
+
+
+@pytest.mark.gpu
+def test_prefill_workspace_size_rule():
+    # P = ceil(2 * SMs / items) parts (at most 8) when the items are fewer than two per SM; then one int
+    # ticket and one int ready count per (sequence, KV head, query tile of 128 / G tokens), each array
+    # padded to 256 bytes, and P records of 128 rows x (128 fp32 + m + l) per item
+    lib = _lib.load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def expect(batch, hq, hkv, max_q):
+        tq = 128 // (hq // hkv)
+        items = batch * hkv * (-(-max_q // tq))
+        if items >= 2 * sms:
+            return 0
+        parts = min(8, -(-2 * sms // items))
+        flags = -(-items * 4 // 256) * 256
+        return 2 * flags + items * parts * (128 * 128 * 4 + 128 * 8)
+
+    for batch, hq, hkv, max_q in [(16, 16, 8, 512), (1, 8, 8, 1), (3, 32, 4, 1000), (1, 16, 8, 512), (2, 32, 8, 300)]:
+        assert lib.pkv_paged_varlen_prefill_workspace_bytes(batch, hq, hkv, 128, max_q) == expect(batch, hq, hkv, max_q)
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "absent.so"))
@@ -128,16 +160,20 @@ def test_argument_errors_return_status():
     assert st == _lib.EALIGN
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
                                            bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 64, 16, 4,
-                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
+                                           ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
     assert st == _lib.EUNSUPPORTED
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
                                            bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 128, 16, 4,
-                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
+                                           ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
     assert st == _lib.EINVAL  # no block tables and no packed k / v
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
                                            bt.data_ptr(), 1, 1, None, 0, 1, -1, 0, 4, 2, 128, 16, 4,
-                                           ctypes.c_float(0.1), 1, _lib.BF16, s)
+                                           ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
     assert st == _lib.EINVAL
+    st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, kc.data_ptr(), kc.data_ptr(),
+                                           bt.data_ptr(), bt.data_ptr(), 1, 1, bt.data_ptr(), 1, 1, 2, 0, 4, 2, 128,
+                                           16, 4, ctypes.c_float(0.1), 1, q.data_ptr() + 16, 1 << 20, _lib.BF16, s)
+    assert st == _lib.EALIGN  # the workspace must be 256-byte aligned
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 

@@ -106,3 +106,53 @@ def test_prefill_many_short_sequences_repeated():
     w = wl.PrefillWorkload("many-short", 23, 4, 2, 128, bs, B + 8, torch.bfloat16, [cached] * B, [nq] * B, tables)
     for _ in range(3):
         run_prefill(w)
+
+
+def _long_history(seed: int, group: int = 2, block_size: int = 256) -> wl.PrefillWorkload:
+    # histories of up to 12 blocks of 256: the last query tiles need ~50 key tiles of 64,
+    # far past the 16 above which a tile runs as two parts
+    return wl.random_prefill(seed, batch=3, max_new=300, min_new=40, max_cached_blocks=12, block_size=block_size,
+                             num_q_heads=8 * group, num_kv_heads=8, head_dim=128)
+
+
+@pytest.mark.parametrize("group", [2, 4])
+def test_long_items_split_and_unsplit_match_oracle(group):
+    w = _long_history(31 + group, group)
+    split = run_prefill(w)                   # cached workspace: long tiles run as two parts
+    whole = run_prefill(w, workspace=False)  # never split
+    # the two paths differ only in rounding order
+    d = (split["out"].float() - whole["out"].float()).abs().max().item()
+    assert d <= 1.6e-2, d
+
+
+def test_long_items_split_non_causal():
+    w = _long_history(35)
+    run_prefill(w, causal=False)
+
+
+def test_split_workspace_reused_and_left_zeroed():
+    w = _long_history(36)
+    hq, hkv = w.num_q_heads, w.num_kv_heads
+    ws = pkv.prefill_workspace(w.batch, hq, hkv, w.head_dim, max(w.num_new))
+    assert ws is not None
+    outs = [run_prefill(w, workspace=ws)["out"] for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    items = w.batch * hkv * -(-max(w.num_new) // (128 // (hq // hkv)))
+    flags = -(-items * 4 // 256) * 256
+    assert int(ws[: 2 * flags].count_nonzero()) == 0  # tickets and ready flags back at zero
+
+
+def test_single_long_history_runs_as_eight_parts():
+    # one sequence, a 16k-token history and 200 new tokens: 32 work items for a GPU with ~300 CTA slots,
+    # so each query tile (259 key tiles) runs as eight parts
+    w = wl.random_prefill(37, batch=1, max_new=200, min_new=200, max_cached_blocks=64, block_size=256,
+                          num_q_heads=16, num_kv_heads=8, head_dim=128)
+    w.num_cached[0] = 64 * 256
+    w.block_tables[0] = list(range(-(-(64 * 256 + 200) // 256)))
+    w.num_blocks = max(w.num_blocks, len(w.block_tables[0]) + 4)
+    assert pkv.prefill_workspace_bytes(1, 16, 8, 128, 200) > 0
+    split = run_prefill(w)
+    whole = run_prefill(w, workspace=False)
+    d = (split["out"].float() - whole["out"].float()).abs().max().item()
+    assert d <= 1.6e-2, d
