@@ -700,7 +700,9 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
 
   if (warp == nw) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // Every lane issues the copies of its tokens (stage position % 32 == lane):
+    // each token's row is a copy of its own (rows sit at a padded stride), and a
+    // single issuing thread would bound the stage rate for small blocks.
     const uint64_t policy = pkv::l2_evict_first_policy();
     const uint32_t head_row = static_cast<uint32_t>(p.hkv) * D * 2;
     int it = 0;
@@ -709,30 +711,32 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
       for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
         const int s = it % p.stages;
         const uint32_t use = it / p.stages;
-        if (use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
+        if (lane == 0 && use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
+        __syncwarp();
         const int nt = min(p.t_stage, seg.t1 - t);
         unsigned char* ks = stage_base + s * p.stage_bytes;
         unsigned char* vs = ks + p.stage_bytes / 2;
-        for (int tt = t; tt < t + nt;) {
+        int valid = 0;
+        for (int u = lane; u < nt; u += 32) {
+          const int phys = __ldg(table + (t + u) / p.block_size);
+          valid += (phys >= 0 && phys < p.num_blocks) ? 1 : 0;
+        }
+        if (valid > 0) pkv::mbar_expect_tx(&full[s], 2 * valid * head_row);
+        for (int u = lane; u < nt; u += 32) {
+          const int tt = t + u;
           const int blk = tt / p.block_size;
-          const int off = tt - blk * p.block_size;
-          const int n = min(p.block_size - off, t + nt - tt);
           const int phys = __ldg(table + blk);
           if (phys < 0 || phys >= p.num_blocks) {
             pkv::raise_error(p.err, PKV_DERR_BLOCK_RANGE);
-          } else {
-            pkv::mbar_expect_tx(&full[s], 2 * n * head_row);
-            const size_t src0 = (static_cast<size_t>(phys) * p.block_size + off) * head_row;
-            for (int u = 0; u < n; ++u) {
-              const size_t src = src0 + static_cast<size_t>(u) * head_row;
-              const size_t dst = static_cast<size_t>(tt - t + u) * ts;
-              pkv::bulk_g2s(ks + dst, p.k_cache + src, head_row, &full[s], policy);
-              pkv::bulk_g2s(vs + dst, p.v_cache + src, head_row, &full[s], policy);
-            }
+            continue;
           }
-          tt += n;
+          const size_t src = (static_cast<size_t>(phys) * p.block_size + (tt - blk * p.block_size)) * head_row;
+          const size_t dst = static_cast<size_t>(u) * ts;
+          pkv::bulk_g2s(ks + dst, p.k_cache + src, head_row, &full[s], policy);
+          pkv::bulk_g2s(vs + dst, p.v_cache + src, head_row, &full[s], policy);
         }
-        pkv::mbar_arrive(&full[s]);
+        __syncwarp();
+        if (lane == 0) pkv::mbar_arrive(&full[s]);
       }
       return true;
     });
