@@ -459,16 +459,53 @@ def bench_verify(args, device, q_len=4):
                          "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
 
 
-def flush_l2(buf):
-    buf.add_(1)
-
-
-def bench_prefill(args, device):
+def bench_long_context(args, device):
+    """Long-context small-batch split decode: 4 sequences of 32k-131k tokens, block size 16, 32q/8kv."""
     import pagedattention_kv_cache_gb300 as pkv
     from pagedattention_kv_cache_gb300 import metadata as md
     from pagedattention_kv_cache_gb300 import workloads as wl
 
-    p = wl.qwen3_prefill_prefix()
+    w = wl.long_context_decode()
+    t = wl.decode_tensors(w, device)
+    meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+    ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0, device=device)
+    out = torch.empty_like(t["q"])
+    flush = torch.empty(torch.cuda.get_device_properties(device).L2_cache_size // 2, dtype=torch.float32,
+                        device=device)
+    times = []
+    for i in range(args.warmup + max(10, args.steps)):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], meta["block_tables"], meta["context_lens"],
+                              w.scale, workspace=ws, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    assert pkv.device_error() == 0
+    ms = statistics.median(times)
+    nbytes = decode_alg_bytes(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = measured_peaks()[0]
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
+            "kernel": "paged_decode_mma_kernel (G=4), automatic split + fused combine",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def bench_prefill(args, device, p=None):
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    p = p or wl.qwen3_prefill_prefix()
     t = wl.prefill_tensors(p, device)
     meta = md.prefill_metadata(p.block_tables, p.num_cached, p.num_new, p.block_size, always_tables=True)
     gm = md.to_device(meta, device)
@@ -620,6 +657,12 @@ def run_ours(args):
     torch.cuda.empty_cache()
     line["fp8_kv"] = bench_fp8(args, device, world)
     line["verify"] = bench_verify(args, device)
+    line["long_context"] = bench_long_context(args, device)
+    from pagedattention_kv_cache_gb300 import workloads as wl
+    lh = bench_prefill(args, device, wl.long_history_prefill())
+    lh["roofline"] = {"bound": "tensor", "achieved": lh["tflops"], "peak": prefill["roofline"]["peak"],
+                      "unit": "TFLOP/s", "frac": round(lh["tflops"] / prefill["roofline"]["peak"], 4)}
+    line["prefill_long_history"] = lh
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -178,6 +178,18 @@ def qwen3_prefill_prefix(seed: int = 1004, batch: int = 16, chunk: int = 512) ->
                            num_blocks, torch.bfloat16, cached, new, tables)
 
 
+def long_history_prefill(seed: int = 1006, history: int = 16384, chunk: int = 512) -> PrefillWorkload:
+    """One sequence resuming after a long cached history (chunked prefill of a long document):
+    ``history`` tokens cached (a multiple of 256), ``chunk`` new tokens, Qwen3-0.6B heads, block size 256."""
+    rng = np.random.default_rng(seed)
+    bs = 256
+    n = history + chunk
+    num_blocks = 2 * _ceil_div(n, bs)
+    tables = _assign_blocks(rng, [n], bs, num_blocks)
+    return PrefillWorkload(f"qwen3-0.6b-prefill-b1-history{history // 1024}k-chunk{chunk}", seed, 16, 8, 128, bs,
+                           num_blocks, torch.bfloat16, [history], [chunk], tables)
+
+
 def random_prefill(seed: int, *, batch: int, max_new: int, max_cached_blocks: int, block_size: int,
                    num_q_heads: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype = torch.bfloat16,
                    min_new: int = 0, spare_blocks: int = 4) -> PrefillWorkload:
