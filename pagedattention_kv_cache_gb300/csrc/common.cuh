@@ -29,6 +29,14 @@ unsigned int* device_error_word(int* status);  // device address of this device'
 int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
                    uint32_t b2);
 
+// Encodes the 4-D bf16 tensor map of one paged K or V pool [num_blocks,
+// block_size, hkv, 128] whose box is 16 tokens of every KV head and one half
+// (64 elements) of head_dim, ordered (half, head, token) in shared memory with
+// 128-byte swizzle: rows of one head's 16 tokens are 128 bytes apart, so any
+// eight consecutive tokens fill the eight swizzle phases.  block_size must be a
+// multiple of 16.
+int encode_paged_kv_bf16(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------- device side

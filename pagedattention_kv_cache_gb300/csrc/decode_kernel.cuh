@@ -34,7 +34,10 @@
 // warp's rows become (query token, head) pairs; K/V are still read once.
 #pragma once
 
+#include <cuda.h>
+
 #include <cfloat>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -107,6 +110,8 @@ struct Params {
   int t_stage;       // tokens per stage
   int stages;
   size_t stage_bytes;
+  int align;  // split points fall on multiples of this many tokens of a sequence (0 or 1: anywhere)
+  int tma;    // mma kernel: stages filled by 4-D tensor copies of 16-token boxes (block_size % 16 == 0)
 };
 
 // One contiguous piece of work: tokens [t0, t1) of sequence b.
@@ -131,6 +136,10 @@ __device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, vo
     pkv::raise_error(err, PKV_DERR_WAIT_TIMEOUT);
   }
 }
+
+__device__ __forceinline__ int align_tokens(const Params& p) { return p.align > 1 ? p.align : 1; }
+
+__device__ __forceinline__ long long round_up(long long n, int a) { return (n + a - 1) / a * a; }
 
 __device__ __forceinline__ int context_len(const Params& p, int b) {
   const int n = __ldg(p.context_lens + b);
@@ -157,8 +166,9 @@ struct Plan {
 __device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
+  const int A = align_tokens(p);
   long long local = 0;
-  for (int b = tid; b < p.batch; b += nthreads) local += context_len(p, b);
+  for (int b = tid; b < p.batch; b += nthreads) local += round_up(context_len(p, b), A);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) local += __shfl_xor_sync(0xffffffffu, local, off);
   if (tid % 32 == 0) sh[tid / 32] = local;
@@ -167,8 +177,8 @@ __device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
   for (int w = 0; w < nthreads / 32; ++w) total += sh[w];
   __syncthreads();
   const long long grid = gridDim.x;
-  long long per = (total + grid - 1) / grid;
-  if (per < kMinTokensPerCta) per = kMinTokensPerCta;
+  long long per = round_up((total + grid - 1) / grid, A);
+  if (per < kMinTokensPerCta) per = round_up(kMinTokensPerCta, A);
   plan.per = per;
   plan.start = per * blockIdx.x;
   plan.end = plan.start + per < total ? plan.start + per : total;
@@ -180,7 +190,7 @@ __device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
   long long running = 0;
   for (int base = 0; base < p.batch; base += nthreads) {
     const int b = base + tid;
-    const long long n = b < p.batch ? context_len(p, b) : 0;
+    const long long n = b < p.batch ? round_up(context_len(p, b), A) : 0;
     long long incl = n;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -217,7 +227,7 @@ __device__ void plan_fixed(const Params& p, Plan& plan) {
   if (b >= p.batch) return;
   const int n = context_len(p, b);
   if (n == 0) return;
-  const int chunk = (n + S - 1) / S;
+  const int chunk = static_cast<int>(round_up((n + S - 1) / S, align_tokens(p)));
   const int t0 = j * chunk;
   if (t0 >= n) return;
   const int t1 = t0 + chunk < n ? t0 + chunk : n;
@@ -233,19 +243,23 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
     return true;
   }
   if (plan.b_first < 0) return true;
+  // positions run over the flattened contexts, each rounded up to the split
+  // alignment; a part's end is clipped to the sequence's real length
+  const int A = align_tokens(p);
   long long cu = plan.cu_first;
   for (int b = plan.b_first; b < p.batch && cu < plan.end; ++b) {
     const int n = context_len(p, b);
+    const long long np = round_up(n, A);
     if (n > 0) {
       const long long s0 = plan.start > cu ? plan.start : cu;
-      const long long s1 = plan.end < cu + n ? plan.end : cu + n;
+      const long long s1 = plan.end < cu + np ? plan.end : cu + np;
       const int c0 = static_cast<int>(cu / plan.per);
-      const int c1 = static_cast<int>((cu + n - 1) / plan.per);
-      Segment seg{b, n, static_cast<int>(s0 - cu), static_cast<int>(s1 - cu), c1 - c0 + 1, c0 + b,
-                  static_cast<int>(blockIdx.x) + b};
+      const int c1 = static_cast<int>((cu + np - 1) / plan.per);
+      Segment seg{b, n, static_cast<int>(s0 - cu), static_cast<int>(s1 - cu < n ? s1 - cu : n), c1 - c0 + 1,
+                  c0 + b, static_cast<int>(blockIdx.x) + b};
       if (!fn(seg)) return false;
     }
-    cu += n;
+    cu += np;
   }
   return true;
 }
@@ -648,15 +662,33 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate): S = Q K^T with the R rows in
 // the M dimension (rows >= R are zero), online softmax on the accumulator
 // fragments (O rescaled only when a row maximum grows by more than 2^8), and
-// O += P V with P taken straight from the S fragments.  Each token's row of
-// all KV heads is copied to shared memory at a stride padded by 16 bytes, so
-// the eight keys an ldmatrix reads sit in eight different bank groups.
+// O += P V with P taken straight from the S fragments.  The eight keys an
+// ldmatrix reads must sit in eight different bank groups; two stage layouts
+// give that:
+//  * block_size a multiple of 16 (p.tma): a warp's 16 keys lie in one block,
+//    and four tensor copies (K and V, two halves of head_dim) of a 16-token box
+//    of every KV head fill its chunk, 128-byte swizzled, rows of one head's
+//    tokens 128 bytes apart (split points then fall on multiples of 16 tokens);
+//  * otherwise each token's row of all KV heads is its own bulk copy, at a
+//    stride padded by 16 bytes.
 
 constexpr int kMmaTokens = 16;  // keys per consumer warp per stage
-constexpr int kMmaPad = 16;     // bytes after each token row in shared memory
+constexpr int kMmaPad = 16;     // bytes after each token row in shared memory (per-token layout)
+
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(pkv::smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(pkv::smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
 
 template <int G, int QL>
-__global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p) {
+__global__ void __launch_bounds__(288, 1)
+    paged_decode_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v) {
   using T = __nv_bfloat16;
   constexpr int D = 128;
   constexpr int R = G * QL;
@@ -668,10 +700,12 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
   const int warp = tid / 32;
   const int lane = tid % 32;
   const int nw = p.nw;
-  const int ts = p.hkv * D * 2 + kMmaPad;  // shared-memory stride of one token's row
+  const int ts = p.hkv * D * 2 + kMmaPad;  // shared-memory stride of one token's row (per-token layout)
+  const int box_bytes = p.hkv * kMmaTokens * 64 * 2;  // one tensor copy: half of head_dim, 16 tokens, all heads
 
-  unsigned char* stage_base = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+  // stages start on a 1024-byte boundary (the period of the 128-byte swizzle)
+  unsigned char* stage_base = smem + ((1024u - (pkv::smem_u32(smem) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stage_base + p.stages * p.stage_bytes);
   uint64_t* empty = full + kMaxStages;
   long long* sh = reinterpret_cast<long long*>(empty + kMaxStages);
   int* sh_flag = reinterpret_cast<int*>(sh + 64);
@@ -706,6 +740,44 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
     const uint64_t policy = pkv::l2_evict_first_policy();
     const uint32_t head_row = static_cast<uint32_t>(p.hkv) * D * 2;
     int it = 0;
+    if (p.tma) {
+      // lane c < wph loads the c-th 16-token box of a stage: one block, one offset
+      if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+      }
+      for_each_segment(p, plan, [&](const Segment& seg) -> bool {
+        const int32_t* table = p.block_tables + static_cast<size_t>(seg.b) * p.max_blocks;
+        for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
+          const int s = it % p.stages;
+          const uint32_t use = it / p.stages;
+          const int tc = t + lane * kMmaTokens;
+          const bool mine = lane < p.wph && tc < seg.t1;
+          const int blk = tc / p.block_size;
+          const int phys = mine ? __ldg(table + blk) : 0;
+          if (lane == 0 && use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
+          __syncwarp();
+          if (mine) {
+            if (phys < 0 || phys >= p.num_blocks) {
+              pkv::raise_error(p.err, PKV_DERR_BLOCK_RANGE);
+            } else {
+              unsigned char* kd = stage_base + s * p.stage_bytes + lane * 2 * box_bytes;
+              unsigned char* vd = kd + p.stage_bytes / 2;
+              const int off = tc - blk * p.block_size;
+              pkv::mbar_expect_tx(&full[s], 4u * static_cast<uint32_t>(box_bytes));
+              tma_load_4d(kd, &tm_k, 0, off, 0, phys, &full[s], policy);
+              tma_load_4d(kd + box_bytes, &tm_k, 64, off, 0, phys, &full[s], policy);
+              tma_load_4d(vd, &tm_v, 0, off, 0, phys, &full[s], policy);
+              tma_load_4d(vd + box_bytes, &tm_v, 64, off, 0, phys, &full[s], policy);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) pkv::mbar_arrive(&full[s]);
+        }
+        return true;
+      });
+      return;
+    }
     for_each_segment(p, plan, [&](const Segment& seg) -> bool {
       const int32_t* table = p.block_tables + static_cast<size_t>(seg.b) * p.max_blocks;
       for (int t = seg.t0; t < seg.t1; t += p.t_stage, ++it) {
@@ -750,6 +822,19 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
   const int c = lane & 3;
   const int nthreads_c = nw * 32;
   const uint32_t stage_addr = pkv::smem_u32(stage_base);
+  // Lane offsets of the ldmatrix rows inside a warp's chunk: row stride rs,
+  // second half of head_dim at +hs, 16-byte column j at (j ^ x) * 16 where x is
+  // the row's swizzle phase (tensor layout) or 0 (per-token layout).  Every
+  // row an ldmatrix lane addresses has phase lane & 7 (row = 8k + (lane & 7)).
+  const int rs = p.tma ? 128 : ts;
+  const int hs = p.tma ? box_bytes : 128;
+  const uint32_t xr = p.tma ? static_cast<uint32_t>(lane & 7) : 0u;
+  // chunk base (K) of this warp in stage 0, relative to the stage
+  const int cbase = p.tma ? phase * 2 * box_bytes + g * kMmaTokens * 128 : phase * kMmaTokens * ts + g * D * 2;
+  const uint32_t krow = cbase + (lane & 7) * rs;
+  const uint32_t vrow = cbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rs;
+  const uint32_t kj = static_cast<uint32_t>(lane >> 3);
+  const uint32_t vj = static_cast<uint32_t>(lane >> 4);
   int it = 0;
 
   for_each_segment(p, plan, [&](const Segment& seg) -> bool {
@@ -787,13 +872,14 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
       const int tt0 = phase * kMmaTokens;
       const int nv = min(max(nt - tt0, 0), kMmaTokens);  // valid keys of this warp's chunk
       if (nv > 0) {
-        const uint32_t kbase = stage_addr + s * p.stage_bytes + tt0 * ts + g * D * 2;
+        const uint32_t kbase = stage_addr + s * p.stage_bytes;
         const uint32_t vbase = kbase + p.stage_bytes / 2;
         if (nv < kMmaTokens) {
           // V rows past the last key hold stale bytes: zero them so 0 * stale never reaches O
-          unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + tt0 * ts + g * D * 2;
+          unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + cbase;
           for (int idx = lane; idx < (kMmaTokens - nv) * 16; idx += 32)
-            *reinterpret_cast<uint4*>(vrows + (nv + idx / 16) * ts + (idx % 16) * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrows + (nv + idx / 16) * rs + ((idx % 16) / 8) * hs + (idx % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
         }
@@ -808,7 +894,7 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb) {
             uint32_t b[4];
-            pkv::ldsm_x4(kbase + (nb * 8 + (lane & 7)) * ts + (k4 * 4 + (lane >> 3)) * 16, b);
+            pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (k4 >> 1) * hs + ((((k4 & 1) * 4 + kj) ^ xr) << 4), b);
             pkv::mma_bf16_16816(sacc[nb], qf[2 * k4], b[0], b[1]);
             pkv::mma_bf16_16816(sacc[nb], qf[2 * k4 + 1], b[2], b[3]);
           }
@@ -858,7 +944,7 @@ __global__ void __launch_bounds__(288, 1) paged_decode_mma_kernel(const Params p
 #pragma unroll
         for (int jp = 0; jp < 8; ++jp) {
           uint32_t b[4];
-          pkv::ldsm_x4_trans(vbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * ts + (2 * jp + (lane >> 4)) * 16, b);
+          pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
           pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
           pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
         }
@@ -1023,9 +1109,23 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   ls.wph = p.hkv >= 8 ? 1 : 8 / p.hkv;
   ls.nw = p.hkv * ls.wph;
   ls.t_stage = kMmaTokens * ls.wph;
-  const size_t ts = static_cast<size_t>(p.hkv) * 128 * 2 + kMmaPad;
-  ls.stage_bytes = static_cast<size_t>(ls.t_stage) * ts * 2;
-  const size_t misc = 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
+  // tensor-copy layout when every 16-token box lies in one block
+  alignas(64) CUtensorMap maps[2];
+  std::memset(maps, 0, sizeof(maps));
+  p.tma = (p.block_size % kMmaTokens == 0 && p.num_blocks > 0) ? 1 : 0;
+  if (p.tma) {
+    if (pkv::encode_paged_kv_bf16(&maps[0], p.k_cache, p.block_size, p.hkv, p.num_blocks) != PKV_OK ||
+        pkv::encode_paged_kv_bf16(&maps[1], p.v_cache, p.block_size, p.hkv, p.num_blocks) != PKV_OK)
+      return PKV_ECUDA;
+    p.align = kMmaTokens;
+    ls.stage_bytes = static_cast<size_t>(ls.t_stage) * p.hkv * 128 * 2 * 2;
+  } else {
+    p.align = 1;
+    const size_t ts = static_cast<size_t>(p.hkv) * 128 * 2 + kMmaPad;
+    ls.stage_bytes = static_cast<size_t>(ls.t_stage) * ts * 2;
+  }
+  // 1024 bytes of slack put the stages on a swizzle-period boundary
+  const size_t misc = 1024 + 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
                       (ls.wph > 1 ? static_cast<size_t>(ls.nw) * R * (128 + 2) * sizeof(float) : 0);
   const int stages = static_cast<int>((kSmemBudget - misc) / ls.stage_bytes);
   ls.stages = stages > kMaxStages ? kMaxStages : stages;
@@ -1046,7 +1146,7 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   else
     grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
   if (grid == 0) return PKV_OK;
-  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
+  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p, maps[0], maps[1]);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -75,6 +75,20 @@ def test_group_8():
     run_decode(w)
 
 
+# G = 4 runs the tensor-core kernel: block sizes that are multiples of 16 fill
+# its stages with 16-token tensor copies (split points on multiples of 16),
+# others with one copy per token row.  Poisoned caches put NaN in every slot
+# no sequence owns, including the tail of a sequence's last block that a
+# 16-token copy brings in.
+@pytest.mark.parametrize("kv_heads,block_size", [(1, 16), (2, 32), (3, 48), (4, 16), (8, 16), (8, 64), (2, 8),
+                                                 (4, 24), (8, 1)])
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_mma_kernel_stage_layouts(kv_heads, block_size, splits):
+    w = wl.random_decode(60 + kv_heads * 7 + block_size, batch=7, max_ctx=900, min_ctx=1, block_size=block_size,
+                         num_q_heads=4 * kv_heads, num_kv_heads=kv_heads, head_dim=128, dtype=torch.bfloat16)
+    run_decode(w, num_splits=splits, poison=True)
+
+
 def test_long_context_split_decode_full_size():
     r = run_decode(wl.long_context_decode(), gen_device="cuda", check_store=True)
     assert r["stats"]["mean_abs"] < 1e-3

@@ -56,6 +56,15 @@ def test_verify_matches_oracle(q_len, group):
         run_verify(w, q_len, splits)
 
 
+@pytest.mark.parametrize("block_size", [8, 48, 3])
+def test_verify_block_sizes(block_size):
+    # 48: 16-token tensor copies inside a block; 8 and 3: one copy per token row
+    w = wl.random_decode(70 + block_size, batch=6, max_ctx=500, min_ctx=4, block_size=block_size, num_q_heads=8,
+                         num_kv_heads=4, head_dim=128, dtype=torch.bfloat16)
+    for splits in (0, 2):
+        run_verify(w, 4, splits)
+
+
 def test_verify_qwen3_batch32_q4():
     w = wl.qwen3_decode_b32()
     run_verify(w, 4)
