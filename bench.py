@@ -412,7 +412,7 @@ def bench_fp8(args, device, world):
               "decode_tokens_per_s": round(world * w.batch / (ms * 1e-3), 1),
               "roofline": {"bound": "hbm", "achieved": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
                            "unit": "GB/s", "frac": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                           "kernel": "paged_decode_kernel<bf16, e4m3>", "alg_bytes_per_launch": dec_bytes,
+                           "kernel": "paged_decode_mma_kernel<G=2, e4m3>", "alg_bytes_per_launch": dec_bytes,
                            "ms_per_launch": round(dec_ms, 5)},
               "gpu_launches": 2 * L * args.steps}
     del kc, vc

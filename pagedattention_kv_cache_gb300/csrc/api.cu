@@ -88,7 +88,8 @@ int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
 }
 
-int encode_paged_kv_bf16(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks) {
+int encode_paged_kv(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks,
+                    int elem_bytes) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
@@ -97,18 +98,18 @@ int encode_paged_kv_bf16(void* map, const void* base, uint32_t block_size, uint3
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   });
-  if (!g_encode) return PKV_ECUDA;
+  if (!g_encode || (elem_bytes != 1 && elem_bytes != 2)) return PKV_ECUDA;
   // dims innermost first: head_dim, token in block, KV head, block; the
   // token stride (all heads of a token) is larger than the head stride
-  const cuuint64_t row = 128 * 2;
+  const cuuint64_t row = 128 * static_cast<cuuint64_t>(elem_bytes);
   const cuuint64_t dims[4] = {128, block_size, hkv, num_blocks};
   const cuuint64_t strides[3] = {hkv * row, row, static_cast<cuuint64_t>(block_size) * hkv * row};
-  const cuuint32_t box[4] = {64, 16, hkv, 1};
+  const cuuint32_t box[4] = {128u / static_cast<cuuint32_t>(elem_bytes), 16, hkv, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType type = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map), type, 4, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ECUDA;
 }
 

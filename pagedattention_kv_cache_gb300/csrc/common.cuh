@@ -29,13 +29,15 @@ unsigned int* device_error_word(int* status);  // device address of this device'
 int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
                    uint32_t b2);
 
-// Encodes the 4-D bf16 tensor map of one paged K or V pool [num_blocks,
-// block_size, hkv, 128] whose box is 16 tokens of every KV head and one half
-// (64 elements) of head_dim, ordered (half, head, token) in shared memory with
-// 128-byte swizzle: rows of one head's 16 tokens are 128 bytes apart, so any
+// Encodes the 4-D tensor map of one paged K or V pool [num_blocks,
+// block_size, hkv, 128] whose box is 16 tokens of every KV head and 128 bytes
+// of head_dim, ordered (head, token) in shared memory with 128-byte swizzle: rows of one head's 16 tokens are 128 bytes apart, so any
 // eight consecutive tokens fill the eight swizzle phases.  block_size must be a
 // multiple of 16.
-int encode_paged_kv_bf16(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks);
+// elem_bytes: 2 (bf16, box of 64 elements, two copies per 16-token box) or 1
+// (E4M3 codes, box of 128, one copy).
+int encode_paged_kv(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks,
+                    int elem_bytes);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -151,6 +153,30 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d (16x8 fp32) += a (16x16 f16, row) * b (16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two E4M3 codes (low byte first) to an f16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two_codes & 0xffffu)));
+  return h;
+}
+// Byte permute: result byte i = byte sel_i of the eight bytes {b, a} (a's are 0-3).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

@@ -66,6 +66,44 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// d0 += a.lo * b.lo and d1 += a.hi * b.hi, a and b f16 pairs, fp32 sums: the
+// mixed-precision fma of the sm_100 family multiplies the f16 operands exactly
+// and rounds once into fp32, so no f16 -> f32 conversion is issued.
+__device__ __forceinline__ void fma_h2(float& d0, float& d1, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+      "fma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(a), "r"(b));
+}
+
+// d0 += p * v.lo and d1 += p * v.hi (p one f16, v an f16 pair), fp32 sums.
+__device__ __forceinline__ void fma_h1(float& d0, float& d1, uint16_t p, uint32_t v) {
+  asm("{\n\t.reg .f16 v0, v1;\n\t"
+      "mov.b32 {v0, v1}, %2;\n\t"
+      "fma.rn.f32.f16 %0, %3, v0, %0;\n\t"
+      "fma.rn.f32.f16 %1, %3, v1, %1;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(v), "h"(p));
+}
+
+// Sixteen E4M3 codes to eight f16 pairs (exact: every E4M3 value is an f16).
+__device__ __forceinline__ void e4m3x16_to_f16x2(const uint4& c, uint32_t* h) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i]) : "h"(static_cast<uint16_t>(w[i] & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i + 1]) : "h"(static_cast<uint16_t>(w[i] >> 16)));
+  }
+}
+
+// P of an FP8-cache stage is carried as f16 scaled by 2^15 (P <= 1, so no
+// overflow, and weights down to 2^-39 stay representable); the factor comes
+// off with V's scale at the end.
+constexpr float kFp8PScale = 32768.0f;
+
 // Register shape of a consumer warp that holds R query rows (query heads x
 // query tokens) of one KV head.
 template <typename T, int D, int R>
@@ -78,9 +116,14 @@ struct Shape {
   static constexpr int CPL = CHUNKS / LPT;                  // chunks per lane
   static constexpr int EPL = CPL * EPC;                     // elements per lane
   static constexpr int TPW = 32 / LPT;                      // tokens per warp round
-  // rounds per stage per warp: short rows (FP8, or bf16 with head_dim 64) take
-  // more tokens per stage so a stage still moves a useful number of bytes
-  static constexpr int ROUNDS = (ROW_BYTES >= 512 || R >= 5) ? 2 : ((ROW_BYTES <= 128 && R <= 2) ? 8 : 4);
+  // CTAs per SM: an FP8 cache with R <= 2 runs two (the per-byte work is
+  // twice bf16's, and the extra warps hide its latency), everything else one
+  static constexpr int CTAS = (sizeof(T) == 1 && R <= 2) ? 2 : 1;
+  // rounds per stage per warp: short rows (bf16 with head_dim 64) take more
+  // tokens per stage so a stage still moves a useful number of bytes; an FP8
+  // stage stays at four rounds to fit two CTAs' rings in shared memory
+  static constexpr int ROUNDS =
+      (ROW_BYTES >= 512 || R >= 5) ? 2 : ((ROW_BYTES <= 128 && R <= 2 && CTAS == 1) ? 8 : 4);
   static_assert(CPL >= 1, "head row too short for the lane split");
 };
 
@@ -339,10 +382,11 @@ __device__ __forceinline__ void combine_if_last(const Params& p, const Segment& 
 // holds R = G * QL rows: row rho is query token rho / G, head g * G + rho % G.
 // T is the q / out element type, TC the cache's (T, or FP8 E4M3 with scales).
 template <typename T, typename TC, int D, int G, int QL>
-__global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_kernel(const Params p) {
   constexpr int R = G * QL;
   using S = Shape<TC, D, R>;
   constexpr int NQ = S::EPC / Chunk<T>::N;  // q / out chunks per cache chunk
+  constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
   const int rows_per_seq = QL * p.hq;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -432,6 +476,12 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
   for_each_segment(p, plan, [&](const Segment& seg) -> bool {
     // q of the R rows sharing KV head g, pre-scaled into the exp2 domain
     float qr[R][S::EPL];
+    // FP8 cache: q as f16 pairs, each row scaled by a power of two that puts
+    // its largest element in [2^14, 2^15) (exact for every element above
+    // 2^-29 of that maximum); qmul takes the power back off with the softmax
+    // scale
+    uint32_t qh16[R][S::EPL / 2];
+    float qmul[R];
 #pragma unroll
     for (int h = 0; h < R; ++h) {
       const T* qh =
@@ -443,8 +493,24 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
           const uint4 c = __ldg(reinterpret_cast<const uint4*>(qh) + (lig + S::LPT * k) * NQ + u);
           Chunk<T>::unpack(c, &qr[h][k * S::EPC + u * Chunk<T>::N]);
         }
+      if constexpr (kFp8) {
+        float amax = 0.f;
 #pragma unroll
-      for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
+        for (int e = 0; e < S::EPL; ++e) amax = fmaxf(amax, fabsf(qr[h][e]));
+#pragma unroll
+        for (int off = 1; off < S::LPT; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const int ex = amax > 0.f ? min(max(14 - ilogbf(amax), -100), 100) : 0;
+        const float up = ldexpf(1.f, ex);
+        qmul[h] = p.scale_log2 * ldexpf(1.f, -ex);
+#pragma unroll
+        for (int e = 0; e < S::EPL; e += 2) {
+          const __half2 v = __floats2half2_rn(qr[h][e] * up, qr[h][e + 1] * up);
+          qh16[h][e / 2] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
+      }
     }
     float acc[R][S::EPL];
     float m[R], l[R];
@@ -480,16 +546,28 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
           for (int h = 0; h < R; ++h) odd[h] = 0.f;
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
-            float f[S::EPC];
-            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+            if constexpr (kFp8) {
+              uint32_t kh[S::EPC / 2];
+              e4m3x16_to_f16x2(pkv::lds128(row + (lig + S::LPT * k) * 16), kh);
 #pragma unroll
-            for (int h = 0; h < R; ++h)
+              for (int h = 0; h < R; ++h)
 #pragma unroll
-              for (int e = 0; e < S::EPC; e += 2)
-                fma2(dot[h], odd[h], qr[h][k * S::EPC + e], qr[h][k * S::EPC + e + 1], f[e], f[e + 1]);
+                for (int e = 0; e < S::EPC / 2; ++e) fma_h2(dot[h], odd[h], qh16[h][k * S::EPC / 2 + e], kh[e]);
+            } else {
+              float f[S::EPC];
+              Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+#pragma unroll
+              for (int h = 0; h < R; ++h)
+#pragma unroll
+                for (int e = 0; e < S::EPC; e += 2)
+                  fma2(dot[h], odd[h], qr[h][k * S::EPC + e], qr[h][k * S::EPC + e + 1], f[e], f[e + 1]);
+            }
           }
 #pragma unroll
-          for (int h = 0; h < R; ++h) dot[h] += odd[h];
+          for (int h = 0; h < R; ++h) {
+            dot[h] += odd[h];
+            if constexpr (kFp8) dot[h] *= qmul[h];
+          }
         }
 #pragma unroll
         for (int h = 0; h < R; ++h) {
@@ -537,13 +615,26 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
           const unsigned char* row = vs + (static_cast<size_t>(tt) * p.hkv + g) * S::ROW_BYTES;
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
-            float f[S::EPC];
-            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+            if constexpr (kFp8) {
+              uint16_t ph[R];
 #pragma unroll
-            for (int h = 0; h < R; ++h)
+              for (int h = 0; h < R; ++h) ph[h] = __half_as_ushort(__float2half_rn(sc[r][h] * kFp8PScale));
+              uint32_t vh[S::EPC / 2];
+              e4m3x16_to_f16x2(pkv::lds128(row + (lig + S::LPT * k) * 16), vh);
 #pragma unroll
-              for (int e = 0; e < S::EPC; e += 2)
-                fma2(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], sc[r][h], sc[r][h], f[e], f[e + 1]);
+              for (int h = 0; h < R; ++h)
+#pragma unroll
+                for (int e = 0; e < S::EPC / 2; ++e)
+                  fma_h1(acc[h][k * S::EPC + 2 * e], acc[h][k * S::EPC + 2 * e + 1], ph[h], vh[e]);
+            } else {
+              float f[S::EPC];
+              Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
+#pragma unroll
+              for (int h = 0; h < R; ++h)
+#pragma unroll
+                for (int e = 0; e < S::EPC; e += 2)
+                  fma2(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], sc[r][h], sc[r][h], f[e], f[e + 1]);
+            }
           }
         }
       }
@@ -551,12 +642,13 @@ __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
       if (lane == 0) pkv::mbar_arrive(&empty[s]);
     }
 
-    // V's scale is linear in the output: apply it once to the accumulators
-    if constexpr (!std::is_same<TC, T>::value) {
+    // V's scale (and P's 2^15) is linear in the output: apply it once to the accumulators
+    if constexpr (kFp8) {
+      const float vs_out = p.v_scale / kFp8PScale;
 #pragma unroll
       for (int h = 0; h < R; ++h)
 #pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[h][e] *= p.v_scale;
+        for (int e = 0; e < S::EPL; ++e) acc[h][e] *= vs_out;
     }
 
     // reduce the token groups of the warp (m is already warp-uniform)
@@ -685,14 +777,33 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-template <int G, int QL>
+// TC is the cache's element type: bf16, or FP8 E4M3 (one byte, with per-tensor
+// K and V scales).  For FP8 the operands are widened in registers to f16,
+// which holds every E4M3 value exactly, and the MMAs run on f16:
+//  * S = Q K^T: an ldmatrix word of a K row is four consecutive codes,
+//    widened to the pairs (4c, 4c+1) and (4c+2, 4c+3); the k index of each
+//    m16n8k16 step is permuted that way on both operands, so Q's fragments are
+//    loaded in the same order.  Q is f16 after a per-row power-of-two scaling
+//    that puts its largest element in [2^14, 2^15).
+//  * O += P V: P is f16 times 2^7 (the lazy rescale lets P reach 2^8, and
+//    2^15 is f16's top binade); l sums the same rounded weights, so the
+//    factor cancels.  V's B fragment
+//    pairs two keys of one column, so each lane reads 16 consecutive codes of
+//    four key rows and byte-permutes key pairs together; n-tile j, column n
+//    then stands for head_dim index 16 n + j, and a lane's accumulators cover
+//    32 consecutive outputs.
+template <int G, int QL, typename TC = __nv_bfloat16>
 __global__ void __launch_bounds__(288, 1)
     paged_decode_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
   using T = __nv_bfloat16;
+  constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
+  constexpr int ES = static_cast<int>(sizeof(TC));  // bytes per cache element
+  constexpr int NH = ES;                             // tensor copies per K (or V) box: 128-byte rows
   constexpr int D = 128;
   constexpr int R = G * QL;
   static_assert(R <= 16, "at most 16 rows per KV head");
+  constexpr int HH = R <= 8 ? 1 : 2;  // fragment row halves (r0, r0 + 8) that hold query rows
   constexpr float kRescale = 8.0f;
   const int rows_per_seq = QL * p.hq;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -700,8 +811,8 @@ __global__ void __launch_bounds__(288, 1)
   const int warp = tid / 32;
   const int lane = tid % 32;
   const int nw = p.nw;
-  const int ts = p.hkv * D * 2 + kMmaPad;  // shared-memory stride of one token's row (per-token layout)
-  const int box_bytes = p.hkv * kMmaTokens * 64 * 2;  // one tensor copy: half of head_dim, 16 tokens, all heads
+  const int ts = p.hkv * D * ES + kMmaPad;  // shared-memory stride of one token's row (per-token layout)
+  const int box_bytes = p.hkv * kMmaTokens * 128;  // one tensor copy: 128-byte rows, 16 tokens, all heads
 
   // stages start on a 1024-byte boundary (the period of the 128-byte swizzle)
   unsigned char* stage_base = smem + ((1024u - (pkv::smem_u32(smem) & 1023u)) & 1023u);
@@ -738,7 +849,7 @@ __global__ void __launch_bounds__(288, 1)
     // each token's row is a copy of its own (rows sit at a padded stride), and a
     // single issuing thread would bound the stage rate for small blocks.
     const uint64_t policy = pkv::l2_evict_first_policy();
-    const uint32_t head_row = static_cast<uint32_t>(p.hkv) * D * 2;
+    const uint32_t head_row = static_cast<uint32_t>(p.hkv) * D * ES;
     int it = 0;
     if (p.tma) {
       // lane c < wph loads the c-th 16-token box of a stage: one block, one offset
@@ -761,14 +872,15 @@ __global__ void __launch_bounds__(288, 1)
             if (phys < 0 || phys >= p.num_blocks) {
               pkv::raise_error(p.err, PKV_DERR_BLOCK_RANGE);
             } else {
-              unsigned char* kd = stage_base + s * p.stage_bytes + lane * 2 * box_bytes;
+              unsigned char* kd = stage_base + s * p.stage_bytes + lane * NH * box_bytes;
               unsigned char* vd = kd + p.stage_bytes / 2;
               const int off = tc - blk * p.block_size;
-              pkv::mbar_expect_tx(&full[s], 4u * static_cast<uint32_t>(box_bytes));
-              tma_load_4d(kd, &tm_k, 0, off, 0, phys, &full[s], policy);
-              tma_load_4d(kd + box_bytes, &tm_k, 64, off, 0, phys, &full[s], policy);
-              tma_load_4d(vd, &tm_v, 0, off, 0, phys, &full[s], policy);
-              tma_load_4d(vd + box_bytes, &tm_v, 64, off, 0, phys, &full[s], policy);
+              pkv::mbar_expect_tx(&full[s], 2u * NH * static_cast<uint32_t>(box_bytes));
+#pragma unroll
+              for (int hh = 0; hh < NH; ++hh) {
+                tma_load_4d(kd + hh * box_bytes, &tm_k, 64 * hh, off, 0, phys, &full[s], policy);
+                tma_load_4d(vd + hh * box_bytes, &tm_v, 64 * hh, off, 0, phys, &full[s], policy);
+              }
             }
           }
           __syncwarp();
@@ -830,16 +942,23 @@ __global__ void __launch_bounds__(288, 1)
   const int hs = p.tma ? box_bytes : 128;
   const uint32_t xr = p.tma ? static_cast<uint32_t>(lane & 7) : 0u;
   // chunk base (K) of this warp in stage 0, relative to the stage
-  const int cbase = p.tma ? phase * 2 * box_bytes + g * kMmaTokens * 128 : phase * kMmaTokens * ts + g * D * 2;
+  const int cbase = p.tma ? phase * NH * box_bytes + g * kMmaTokens * 128 : phase * kMmaTokens * ts + g * D * ES;
   const uint32_t krow = cbase + (lane & 7) * rs;
   const uint32_t vrow = cbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rs;
   const uint32_t kj = static_cast<uint32_t>(lane >> 3);
   const uint32_t vj = static_cast<uint32_t>(lane >> 4);
+  // FP8 V: this lane reads 16 codes (chunk lane / 4) of key rows 2c, 2c + 1 and
+  // the same + 8; a row's swizzle phase is key & 7
+  const uint32_t vq = static_cast<uint32_t>(lane >> 2);
+  const uint32_t v8a = cbase + (2 * c) * rs + ((vq ^ (p.tma ? 2u * c : 0u)) << 4);
+  const uint32_t v8b = cbase + (2 * c + 1) * rs + ((vq ^ (p.tma ? 2u * c + 1u : 0u)) << 4);
   int it = 0;
 
   for_each_segment(p, plan, [&](const Segment& seg) -> bool {
     // Q as the A operand: rows r0 / r0 + 8, columns 16 kk + 2c (+1) and + 8
+    // (bf16), or 16 kk + 4c (+1) and 16 kk + 4c + 2 (+3) as scaled f16 (FP8)
     uint32_t qf[8][4];
+    float qmul[2] = {p.scale_log2, p.scale_log2};
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int rho = r0 + 8 * hh;
@@ -848,10 +967,36 @@ __global__ void __launch_bounds__(288, 1)
                                                       ((static_cast<size_t>(seg.b) * QL + rho / G) * p.hq + g * G +
                                                        rho % G) * D)
                   : nullptr;
+      if constexpr (kFp8) {
+        float amax = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qf[kk][hh] = qrow ? __ldg(qrow + kk * 8 + c) : 0u;
-        qf[kk][2 + hh] = qrow ? __ldg(qrow + kk * 8 + 4 + c) : 0u;
+        for (int kk = 0; kk < 8; ++kk) {
+          qf[kk][hh] = qrow ? __ldg(qrow + kk * 8 + 2 * c) : 0u;
+          qf[kk][2 + hh] = qrow ? __ldg(qrow + kk * 8 + 2 * c + 1) : 0u;
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(qf[kk][hh] << 16)),
+                                         fabsf(__uint_as_float(qf[kk][hh] & 0xffff0000u))),
+                                   fmaxf(fabsf(__uint_as_float(qf[kk][2 + hh] << 16)),
+                                         fabsf(__uint_as_float(qf[kk][2 + hh] & 0xffff0000u)))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int ex = amax > 0.f ? min(max(14 - ilogbf(amax), -100), 100) : 0;
+        const float up = ldexpf(1.f, ex);
+        qmul[hh] = p.scale_log2 * ldexpf(1.f, -ex);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t x = qf[kk][2 * w + hh];
+            qf[kk][2 * w + hh] =
+                pkv::pack_f16x2(__uint_as_float(x << 16) * up, __uint_as_float(x & 0xffff0000u) * up);
+          }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qf[kk][hh] = qrow ? __ldg(qrow + kk * 8 + c) : 0u;
+          qf[kk][2 + hh] = qrow ? __ldg(qrow + kk * 8 + 4 + c) : 0u;
+        }
       }
     }
     const int lim0 = seg.ctx - QL + (r0 < R ? r0 / G : 0);
@@ -876,9 +1021,10 @@ __global__ void __launch_bounds__(288, 1)
         const uint32_t vbase = kbase + p.stage_bytes / 2;
         if (nv < kMmaTokens) {
           // V rows past the last key hold stale bytes: zero them so 0 * stale never reaches O
+          constexpr int CPR = 8 * NH;  // 16-byte chunks of one head's row
           unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + cbase;
-          for (int idx = lane; idx < (kMmaTokens - nv) * 16; idx += 32)
-            *reinterpret_cast<uint4*>(vrows + (nv + idx / 16) * rs + ((idx % 16) / 8) * hs + (idx % 8) * 16) =
+          for (int idx = lane; idx < (kMmaTokens - nv) * CPR; idx += 32)
+            *reinterpret_cast<uint4*>(vrows + (nv + idx / CPR) * rs + ((idx % CPR) / 8) * hs + (idx % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -889,31 +1035,48 @@ __global__ void __launch_bounds__(288, 1)
         for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[nb][e] = 0.f;
+        if constexpr (kFp8) {
+          // a word of four codes widens to the B pairs of one k16 step
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
+          for (int q4 = 0; q4 < 2; ++q4) {
 #pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            uint32_t b[4];
-            pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (k4 >> 1) * hs + ((((k4 & 1) * 4 + kj) ^ xr) << 4), b);
-            pkv::mma_bf16_16816(sacc[nb], qf[2 * k4], b[0], b[1]);
-            pkv::mma_bf16_16816(sacc[nb], qf[2 * k4 + 1], b[2], b[3]);
+            for (int nb = 0; nb < 2; ++nb) {
+              uint32_t b[4];
+              pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (((q4 * 4 + kj) ^ xr) << 4), b);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                pkv::mma_f16_16816(sacc[nb], qf[4 * q4 + i], pkv::e4m3x2_to_f16x2(b[i]),
+                                   pkv::e4m3x2_to_f16x2(b[i] >> 16));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+              uint32_t b[4];
+              pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (k4 >> 1) * hs + ((((k4 & 1) * 4 + kj) ^ xr) << 4), b);
+              pkv::mma_bf16_16816(sacc[nb], qf[2 * k4], b[0], b[1]);
+              pkv::mma_bf16_16816(sacc[nb], qf[2 * k4 + 1], b[2], b[3]);
+            }
           }
         }
-        // scale, mask, online softmax per row (lazy rescale of O)
+        // scale, mask, online softmax per row (lazy rescale of O); with R <= 8
+        // the fragment rows r0 + 8 hold no query row and are skipped (P = 0)
         float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 2 * HH; ++e) {
             const int key = nb * 8 + 2 * c + (e & 1);
-            float x = sacc[nb][e] * p.scale_log2;
+            float x = sacc[nb][e] * qmul[e >> 1];
             const bool visible = key < nv && (QL == 1 || t + tt0 + key <= ((e < 2) ? lim0 : lim1));
             x = visible ? x : -INFINITY;
             sacc[nb][e] = x;
             mt[e >> 1] = fmaxf(mt[e >> 1], x);
           }
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < HH; ++hh) {
           mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 1));
           mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 2));
           const float mn = fmaxf(m[hh], mt[hh]);
@@ -931,22 +1094,58 @@ __global__ void __launch_bounds__(288, 1)
         const float mu0 = m[0] == -INFINITY ? 0.f : m[0];
         const float mu1 = m[1] == -INFINITY ? 0.f : m[1];
         uint32_t pf[4];
+        if constexpr (kFp8) {
+          // P as f16 times 2^7; l sums the same rounded weights
+          constexpr float kPs = 128.0f;
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(exp2f(sacc[nb][0] - mu0), exp2f(sacc[nb][1] - mu0));
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(exp2f(sacc[nb][2] - mu1), exp2f(sacc[nb][3] - mu1));
-          l[0] += __low2float(lo) + __high2float(lo);
-          l[1] += __low2float(hi) + __high2float(hi);
-          pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
-          pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
-        // O += P V over the 16 keys: 16 n-tiles of 8 columns
+          for (int nb = 0; nb < 2; ++nb) {
+            const __half2 lo = __floats2half2_rn(exp2f(sacc[nb][0] - mu0) * kPs, exp2f(sacc[nb][1] - mu0) * kPs);
+            l[0] += __low2float(lo) + __high2float(lo);
+            pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
+            pf[2 * nb + 1] = 0u;
+            if constexpr (HH == 2) {
+              const __half2 hi = __floats2half2_rn(exp2f(sacc[nb][2] - mu1) * kPs, exp2f(sacc[nb][3] - mu1) * kPs);
+              l[1] += __low2float(hi) + __high2float(hi);
+              pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+          }
+          // O += P V: pair keys (2c, 2c+1) and (2c+8, 2c+9) of one column by byte permutes
+          const uint4 ra = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a);
+          const uint4 rb = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8b);
+          const uint4 rc = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a + 8 * rs);
+          const uint4 rd = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8b + 8 * rs);
+          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+          const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
 #pragma unroll
-        for (int jp = 0; jp < 8; ++jp) {
-          uint32_t b[4];
-          pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
-          pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
-          pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t x01 = pkv::prmt(wa[i], wb[i], 0x5140u), x23 = pkv::prmt(wa[i], wb[i], 0x7362u);
+            const uint32_t y01 = pkv::prmt(wc[i], wd[i], 0x5140u), y23 = pkv::prmt(wc[i], wd[i], 0x7362u);
+            pkv::mma_f16_16816(o[4 * i], pf, pkv::e4m3x2_to_f16x2(x01), pkv::e4m3x2_to_f16x2(y01));
+            pkv::mma_f16_16816(o[4 * i + 1], pf, pkv::e4m3x2_to_f16x2(x01 >> 16), pkv::e4m3x2_to_f16x2(y01 >> 16));
+            pkv::mma_f16_16816(o[4 * i + 2], pf, pkv::e4m3x2_to_f16x2(x23), pkv::e4m3x2_to_f16x2(y23));
+            pkv::mma_f16_16816(o[4 * i + 3], pf, pkv::e4m3x2_to_f16x2(x23 >> 16), pkv::e4m3x2_to_f16x2(y23 >> 16));
+          }
+        } else {
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(exp2f(sacc[nb][0] - mu0), exp2f(sacc[nb][1] - mu0));
+            l[0] += __low2float(lo) + __high2float(lo);
+            pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
+            pf[2 * nb + 1] = 0u;
+            if constexpr (HH == 2) {
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(exp2f(sacc[nb][2] - mu1), exp2f(sacc[nb][3] - mu1));
+              l[1] += __low2float(hi) + __high2float(hi);
+              pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+          }
+          // O += P V over the 16 keys: 16 n-tiles of 8 columns
+#pragma unroll
+          for (int jp = 0; jp < 8; ++jp) {
+            uint32_t b[4];
+            pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
+            pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
+            pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+          }
         }
       }
       __syncwarp();
@@ -1017,7 +1216,31 @@ __global__ void __launch_bounds__(288, 1)
         const int rho = r0 + 8 * hh;
         if (rho >= R) continue;
         const int head = (rho / G) * p.hq + g * G + rho % G;
-        if (seg.nparts == 1) {
+        if constexpr (kFp8) {
+          // accumulator (j, 2c + e) is output 32c + 16e + j; V's scale comes off here
+          // (P's 2^7 cancels against l)
+          const float ws = seg.nparts == 1 ? p.v_scale / l[hh] : p.v_scale;
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            f[j] = o[j][2 * hh] * ws;
+            f[16 + j] = o[j][2 * hh + 1] * ws;
+          }
+          if (seg.nparts == 1) {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
+                                                   (static_cast<size_t>(seg.b) * rows_per_seq + head) * D + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              orow[u] = make_uint4(pkv::pack_bf16x2(f[8 * u], f[8 * u + 1]), pkv::pack_bf16x2(f[8 * u + 2], f[8 * u + 3]),
+                                   pkv::pack_bf16x2(f[8 * u + 4], f[8 * u + 5]),
+                                   pkv::pack_bf16x2(f[8 * u + 6], f[8 * u + 7]));
+          } else {
+            float4* po = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D +
+                                                   32 * c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) po[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
+          }
+        } else if (seg.nparts == 1) {
           const float inv = 1.f / l[hh];
           uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
                                                        (static_cast<size_t>(seg.b) * rows_per_seq + head) * D);
@@ -1028,6 +1251,8 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             *reinterpret_cast<float2*>(po + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
+        }
+        if (seg.nparts > 1) {
           if (c == 0)
             *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
                 make_float2(m[hh], l[hh]);
@@ -1056,7 +1281,7 @@ LaunchShape launch_shape(int hkv) {
   ls.stage_bytes = static_cast<size_t>(ls.t_stage) * hkv * S::ROW_BYTES * 2;
   const size_t misc = 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
                       (ls.wph > 1 ? static_cast<size_t>(ls.nw) * R * (D + 2) * sizeof(float) : 0);
-  int stages = static_cast<int>((kSmemBudget - misc) / ls.stage_bytes);
+  int stages = static_cast<int>((kSmemBudget / S::CTAS - misc) / ls.stage_bytes);
   ls.stages = stages > kMaxStages ? kMaxStages : stages;
   ls.smem = ls.stages * ls.stage_bytes + misc;
   return ls;
@@ -1096,14 +1321,15 @@ int launch(Params& p, int sms, cudaStream_t stream) {
   if (p.num_splits > 0)
     grid = static_cast<unsigned>(static_cast<long long>(p.batch) * p.num_splits);
   else
-    grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
+    grid = static_cast<unsigned>(sms * kAutoCtasPerSm * Shape<TC, D, G * QL>::CTAS);
   if (grid == 0) return PKV_OK;
   kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-template <int G, int QL>
+template <int G, int QL, typename TC = __nv_bfloat16>
 int launch_mma(Params& p, int sms, cudaStream_t stream) {
+  constexpr int ES = static_cast<int>(sizeof(TC));
   constexpr int R = G * QL;
   LaunchShape ls;
   ls.wph = p.hkv >= 8 ? 1 : 8 / p.hkv;
@@ -1114,14 +1340,14 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   std::memset(maps, 0, sizeof(maps));
   p.tma = (p.block_size % kMmaTokens == 0 && p.num_blocks > 0) ? 1 : 0;
   if (p.tma) {
-    if (pkv::encode_paged_kv_bf16(&maps[0], p.k_cache, p.block_size, p.hkv, p.num_blocks) != PKV_OK ||
-        pkv::encode_paged_kv_bf16(&maps[1], p.v_cache, p.block_size, p.hkv, p.num_blocks) != PKV_OK)
+    if (pkv::encode_paged_kv(&maps[0], p.k_cache, p.block_size, p.hkv, p.num_blocks, ES) != PKV_OK ||
+        pkv::encode_paged_kv(&maps[1], p.v_cache, p.block_size, p.hkv, p.num_blocks, ES) != PKV_OK)
       return PKV_ECUDA;
     p.align = kMmaTokens;
-    ls.stage_bytes = static_cast<size_t>(ls.t_stage) * p.hkv * 128 * 2 * 2;
+    ls.stage_bytes = static_cast<size_t>(ls.t_stage) * p.hkv * 128 * ES * 2;
   } else {
     p.align = 1;
-    const size_t ts = static_cast<size_t>(p.hkv) * 128 * 2 + kMmaPad;
+    const size_t ts = static_cast<size_t>(p.hkv) * 128 * ES + kMmaPad;
     ls.stage_bytes = static_cast<size_t>(ls.t_stage) * ts * 2;
   }
   // 1024 bytes of slack put the stages on a swizzle-period boundary
@@ -1136,7 +1362,7 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   p.t_stage = ls.t_stage;
   p.stages = ls.stages;
   p.stage_bytes = ls.stage_bytes;
-  auto kernel = paged_decode_mma_kernel<G, QL>;
+  auto kernel = paged_decode_mma_kernel<G, QL, TC>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ls.smem)) !=
       cudaSuccess)
     return PKV_ECUDA;

@@ -48,12 +48,47 @@ def _quantized_pool(shape, gen, scale):
 @pytest.mark.parametrize("group", [1, 2, 4])
 @pytest.mark.parametrize("splits", [0, 1, 5])
 def test_fp8_decode_matches_oracle_on_dequantized_cache(group, splits):
-    w = wl.random_decode(60 + group, batch=12, max_ctx=1200, min_ctx=0, block_size=16, num_q_heads=4 * group,
-                         num_kv_heads=4, head_dim=128, dtype=torch.bfloat16)
+    _fp8_decode_case(group, splits, 1.0)
+
+
+# q far outside f16's range either way: both kernels carry q in f16 after a
+# per-row power-of-two scaling, which must leave the scores unchanged
+@pytest.mark.parametrize("group", [2, 4])
+@pytest.mark.parametrize("q_scale", [1e-6, 3e4, 1e9])
+def test_fp8_decode_q_magnitudes(group, q_scale):
+    _fp8_decode_case(group, 0, q_scale)
+
+
+# G = 4 runs the tensor-core kernel: 16-token tensor copies when the block size
+# is a multiple of 16, one copy per token row otherwise.  Every code outside
+# the contexts is the E4M3 NaN (0x7f), including the tail of a sequence's last
+# block that a 16-token copy brings in.
+@pytest.mark.parametrize("kv_heads,block_size", [(1, 16), (2, 8), (3, 48), (8, 16), (8, 32), (4, 5)])
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_fp8_decode_group4_layouts(kv_heads, block_size, splits):
+    _fp8_decode_case(4, splits, 1.0, kv_heads=kv_heads, block_size=block_size, poison=True)
+
+
+def _poison_codes(pool, tables, lens, block_size):
+    used = torch.zeros(pool.shape[0], block_size, dtype=torch.bool)
+    for table, n in zip(tables, lens):
+        for j, block in enumerate(table):
+            used[block, : max(0, min(block_size, n - j * block_size))] = True
+    pool[~used] = 0x7F
+
+
+def _fp8_decode_case(group, splits, q_scale, kv_heads=4, block_size=16, poison=False):
+    w = wl.random_decode(60 + group + 7 * kv_heads + block_size, batch=12, max_ctx=1200, min_ctx=0,
+                         block_size=block_size, num_q_heads=group * kv_heads, num_kv_heads=kv_heads, head_dim=128,
+                         dtype=torch.bfloat16)
     gen = torch.Generator().manual_seed(group)
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
     kc, vc = _quantized_pool(shape, gen, K_SCALE), _quantized_pool(shape, gen, V_SCALE)
-    q = torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+    if poison:
+        # the new token's slot (position len - 1) is written by the store below
+        for pool in (kc, vc):
+            _poison_codes(pool, w.block_tables, [max(0, n - 1) for n in w.context_lens], w.block_size)
+    q = (torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen) * q_scale).to(torch.bfloat16)
     kn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
     vn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
     meta = md.decode_metadata(w.block_tables, w.context_lens, w.block_size)
