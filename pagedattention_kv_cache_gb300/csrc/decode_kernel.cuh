@@ -309,14 +309,16 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
 
 // Called by all consumer threads after this CTA wrote its part of a split
 // sequence: the part that arrives last (atomic ticket, nothing waits) merges
-// every part's (o, m, l) by log-sum-exp and writes the output.  One warp per
-// output row: lanes reduce the row's maximum and denominator over the parts
-// with shuffles, then each lane owns D / 32 columns and sums the parts eight
-// at a time, so a long context split over dozens of CTAs merges in a few
-// round trips to L2.
+// every part's (o, m, l) by log-sum-exp and writes the output.  A warp takes
+// four output rows at a time so their loads overlap: one pass over the parts
+// folds each lane's share of (m, l) online and the lanes combine them by
+// shuffles; a second pass sums the weighted rows, each lane owning D / 32
+// columns, eight parts per step.  A long context split over dozens of CTAs
+// then merges in a few round trips to L2 instead of a few per row.
 template <typename T, int D>
 __device__ __forceinline__ void combine_if_last(const Params& p, const Segment& seg, int rows_per_seq, int* sh_flag,
                                                 int nthreads_c) {
+  constexpr int RW = 4;  // rows a warp merges together
   const int tid = threadIdx.x;
   pkv::named_barrier_sync(1, nthreads_c);
   if (tid == 0) {
@@ -330,48 +332,82 @@ __device__ __forceinline__ void combine_if_last(const Params& p, const Segment& 
     constexpr int PER = D / 32;
     const int warp = tid / 32;
     const int lane = tid % 32;
+    const int nwarps = nthreads_c / 32;
     const int np = seg.nparts;
     T* out = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
-    for (int row = warp; row < rows_per_seq; row += nthreads_c / 32) {
-      const float* ml_row = p.part_ml + (static_cast<size_t>(seg.first_slot) * rows_per_seq + row) * 2;
-      const size_t ml_stride = static_cast<size_t>(rows_per_seq) * 2;
-      float mm = -INFINITY;
-      for (int j = lane; j < np; j += 32) mm = fmaxf(mm, __ldcg(ml_row + j * ml_stride));
+    const size_t ml_stride = static_cast<size_t>(rows_per_seq) * 2;
+    const size_t o_stride = static_cast<size_t>(rows_per_seq) * D;
+    const float* ml_base = p.part_ml + static_cast<size_t>(seg.first_slot) * rows_per_seq * 2;
+    const float* o_base = p.part_o + static_cast<size_t>(seg.first_slot) * rows_per_seq * D + lane * PER;
+    for (int row0 = warp * RW; row0 < rows_per_seq; row0 += nwarps * RW) {
+      float mm[RW], ll[RW];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-      float ll = 0.f;
+      for (int r = 0; r < RW; ++r) {
+        mm[r] = -INFINITY;
+        ll[r] = 0.f;
+      }
+      // (m, l) of this lane's parts, folded online
       for (int j = lane; j < np; j += 32) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_row + j * ml_stride));
-        ll += exp2f(v.x - mm) * v.y;
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+          if (row0 + r >= rows_per_seq) continue;
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_base + j * ml_stride + (row0 + r) * 2));
+          const float mn = fmaxf(mm[r], v.x);
+          if (mn != -INFINITY) {
+            ll[r] = ll[r] * exp2f(mm[r] - mn) + v.y * exp2f(v.x - mn);
+            mm[r] = mn;
+          }
+        }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, off);
-      const float inv = 1.f / ll;
-      const float* o_row = p.part_o + (static_cast<size_t>(seg.first_slot) * rows_per_seq + row) * D + lane * PER;
-      const size_t o_stride = static_cast<size_t>(rows_per_seq) * D;
-      float acc[PER];
+      for (int r = 0; r < RW; ++r) {
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+        for (int off = 16; off > 0; off >>= 1) {
+          const float mo = __shfl_xor_sync(0xffffffffu, mm[r], off);
+          const float lo = __shfl_xor_sync(0xffffffffu, ll[r], off);
+          const float mn = fmaxf(mm[r], mo);
+          if (mn != -INFINITY) {
+            ll[r] = ll[r] * exp2f(mm[r] - mn) + lo * exp2f(mo - mn);
+            mm[r] = mn;
+          }
+        }
+      }
+      float acc[RW][PER];
+#pragma unroll
+      for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[r][e] = 0.f;
 #pragma unroll 8
       for (int j = 0; j < np; ++j) {
-        const float w = exp2f(__ldcg(ml_row + j * ml_stride) - mm);
-        float v[PER];
-        if constexpr (PER == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(o_row + j * o_stride));
-          v[0] = x.x;
-          v[1] = x.y;
-          v[2] = x.z;
-          v[3] = x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(o_row + j * o_stride));
-          v[0] = x.x;
-          v[1] = x.y;
-        }
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+        for (int r = 0; r < RW; ++r) {
+          if (row0 + r >= rows_per_seq) continue;
+          const float w = exp2f(__ldcg(ml_base + j * ml_stride + (row0 + r) * 2) - mm[r]);
+          const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
+          float v[PER];
+          if constexpr (PER == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+            v[0] = x.x;
+            v[1] = x.y;
+            v[2] = x.z;
+            v[3] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            v[0] = x.x;
+            v[1] = x.y;
+          }
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[e], acc[r][e]);
+        }
       }
 #pragma unroll
-      for (int e = 0; e < PER; ++e) out[static_cast<size_t>(row) * D + lane * PER + e] = static_cast<T>(acc[e] * inv);
+      for (int r = 0; r < RW; ++r) {
+        if (row0 + r >= rows_per_seq) continue;
+        const float inv = 1.f / ll[r];
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          out[static_cast<size_t>(row0 + r) * D + lane * PER + e] = static_cast<T>(acc[r][e] * inv);
+      }
     }
     if (tid == 0) p.counters[seg.b] = 0;
   }
