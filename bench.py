@@ -686,6 +686,26 @@ def run_profile_case(args):
         st = DecodeState(w, device)
         for _ in range(3):
             st.step()
+    elif args.profile == "decode-fp8":
+        # one layer of the FP8 bench step at batch 64 (about 0.6 GB of codes)
+        w = wl.qwen3_decode_b256_28l(batch=64, num_layers=1)
+        shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed * 7)
+        kc, vc = [(torch.randn(shape, generator=gen, device=device) / s).clamp_(-448, 448).to(torch.float8_e4m3fn)
+                  .view(torch.uint8) for s in (FP8_K_SCALE, FP8_V_SCALE)]
+        q = torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen, device=device).bfloat16()
+        meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+        for _ in range(3):
+            pkv.paged_decode_attn_fp8(q, kc, vc, meta["block_tables"], meta["context_lens"], w.scale, FP8_K_SCALE,
+                                      FP8_V_SCALE)
+    elif args.profile == "verify":
+        w = wl.qwen3_decode_b256_28l(batch=64, num_layers=1)
+        t = wl.verify_tensors(w, 4, device)
+        meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+        for _ in range(3):
+            pkv.paged_verify_attn(t["q"], t["k_cache"], t["v_cache"], meta["block_tables"], meta["context_lens"],
+                                  w.scale)
     elif args.profile == "prefill":
         p = wl.qwen3_prefill_prefix()
         t = wl.prefill_tensors(p, device)
@@ -709,7 +729,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode-long", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "decode-long", "decode-fp8", "verify", "prefill"],
                     help="run a small single-kernel case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
