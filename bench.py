@@ -431,8 +431,7 @@ def bench_verify(args, device, q_len=4):
     meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
     ws = pkv.decode_workspace(w.batch, q_len * w.num_q_heads, w.head_dim, 0, device=device)
     out = torch.empty_like(t["q"])
-    flush = torch.empty(torch.cuda.get_device_properties(device).L2_cache_size // 2, dtype=torch.float32,
-                        device=device)
+    flush = L2Flush(device)
     times = []
     for i in range(args.warmup + max(10, args.steps)):
         flush_l2(flush)
@@ -470,8 +469,7 @@ def bench_long_context(args, device):
     meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
     ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0, device=device)
     out = torch.empty_like(t["q"])
-    flush = torch.empty(torch.cuda.get_device_properties(device).L2_cache_size // 2, dtype=torch.float32,
-                        device=device)
+    flush = L2Flush(device)
     times = []
     for i in range(args.warmup + max(10, args.steps)):
         flush_l2(flush)
@@ -496,8 +494,75 @@ def bench_long_context(args, device):
                          "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
 
 
-def flush_l2(buf):
-    buf.add_(1)
+def bench_kv_store(args, device):
+    """kv_store at the prefill batch's size (7,168 new tokens, L2 flushed) and at 65,536 tokens
+    (537 MB moved: the HBM roofline case), both bf16, 8 KV heads, head_dim 128."""
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    hbm_peak = measured_peaks()[0]
+    flush = L2Flush(device)
+    result = {}
+    p = wl.qwen3_prefill_prefix()
+    t = wl.prefill_tensors(p, device)
+    meta = md.prefill_metadata(p.block_tables, p.num_cached, p.num_new, p.block_size, always_tables=True)
+    cases = [("prefill_batch", t["k"], t["v"], t["k_cache"], t["v_cache"],
+              torch.from_numpy(meta["slot_mapping"]).to(device))]
+    n_big = 65536
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1007)
+    bs, hkv, d = 16, 8, 128
+    nblk = n_big // bs + 64
+    kc = torch.empty(nblk, bs, hkv, d, dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    slots = torch.randperm(nblk * bs, generator=gen, device=device)[:n_big].to(torch.int32)
+    kb = torch.randn(n_big, hkv, d, generator=gen, device=device).bfloat16()
+    vb = torch.randn(n_big, hkv, d, generator=gen, device=device).bfloat16()
+    cases.append(("65536_tokens", kb, vb, kc, vc, slots))
+    for name, k, v, kcache, vcache, sm in cases:
+        n = k.shape[0]
+        nbytes = 2 * 2 * n * k.shape[1] * k.shape[2] * k.element_size() + 4 * n
+        times = []
+        for i in range(args.warmup + max(10, args.steps)):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pkv.kv_store(k, v, kcache, vcache, sm)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        result[name] = {"tokens": n, "alg_bytes": nbytes, "ms_median": round(ms, 5), "value": round(gbs, 1),
+                        "unit": UNIT, "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                                                   "unit": "GB/s", "frac": round(gbs / hbm_peak, 4)}}
+    assert pkv.device_error() == 0
+    result["l2"] = "flushed before each rep"
+    result["kernel"] = "kv_store_kernel"
+    del t, kc, vc, kb, vb
+    torch.cuda.empty_cache()
+    return result
+
+
+class L2Flush:
+    """Between timed reps: write a buffer twice the size of L2, then read another one as large,
+    so L2 holds none of the timed call's inputs and no dirty lines whose write-back would land
+    inside the next timed call."""
+
+    def __init__(self, device):
+        n = torch.cuda.get_device_properties(device).L2_cache_size // 2  # floats: 2x L2 bytes
+        self.dirty = torch.empty(n, dtype=torch.float32, device=device)
+        self.clean = torch.zeros(n, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.dirty.add_(1)
+        self.clean.sum()
+
+
+def flush_l2(flush):
+    flush()
 
 
 def bench_prefill(args, device, p=None):
@@ -510,8 +575,7 @@ def bench_prefill(args, device, p=None):
     meta = md.prefill_metadata(p.block_tables, p.num_cached, p.num_new, p.block_size, always_tables=True)
     gm = md.to_device(meta, device)
     out = torch.empty_like(t["q"])
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(4 * l2 // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
 
     def run():
         pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], gm["slot_mapping"])
@@ -658,6 +722,7 @@ def run_ours(args):
     line["fp8_kv"] = bench_fp8(args, device, world)
     line["verify"] = bench_verify(args, device)
     line["long_context"] = bench_long_context(args, device)
+    line["kv_store"] = bench_kv_store(args, device)
     from pagedattention_kv_cache_gb300 import workloads as wl
     lh = bench_prefill(args, device, wl.long_history_prefill())
     lh["roofline"] = {"bound": "tensor", "achieved": lh["tflops"], "peak": prefill["roofline"]["peak"],

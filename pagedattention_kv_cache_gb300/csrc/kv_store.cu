@@ -17,28 +17,57 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-// One thread per 16-byte chunk of a token row (all KV heads of the token).
-__global__ void __launch_bounds__(256) kv_store_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+// A token row (all KV heads of the token) is cpr 16-byte chunks.  Lanes are
+// grouped per token: a group of lpt lanes (cpr rounded up to a power of two,
+// at most 32) takes one token, each lane up to kBatch of its chunks per pass.
+// The slot and every chunk of K and V are loaded before anything is stored,
+// so one round trip to memory covers a whole row.
+constexpr int kBatch = 4;
+constexpr int kBlocksPerSm = 4;  // resident blocks of 256 threads at this kernel's register count
+
+__global__ void __launch_bounds__(256, kBlocksPerSm) kv_store_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                                       const int32_t* __restrict__ slot_mapping, int64_t total_chunks,
-                                                       int32_t chunks_per_row, int64_t num_slots,
+                                                       const int32_t* __restrict__ slot_mapping, int32_t num_tokens,
+                                                       int32_t cpr, int32_t lpt, int64_t num_slots,
                                                        unsigned int* err) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total_chunks;
-       idx += stride) {
-    const int64_t token = idx / chunks_per_row;
-    const int32_t chunk = static_cast<int32_t>(idx - token * chunks_per_row);
+  const int lane = threadIdx.x % 32;
+  const int sub = lane / lpt;       // token of this lane inside the warp's group
+  const int cl = lane % lpt;        // first chunk of this lane
+  const int tpw = 32 / lpt;         // tokens per warp pass
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+  for (int64_t t0 = warp * tpw; t0 < num_tokens; t0 += nwarps * tpw) {
+    const int64_t token = t0 + sub;
+    if (token >= num_tokens) continue;
     const int32_t slot = __ldg(slot_mapping + token);
-    if (slot == -1) continue;
-    if (slot < 0 || slot >= num_slots) {
-      if (chunk == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);
-      continue;
+    const uint4* ks = k + token * cpr;
+    const uint4* vs = v + token * cpr;
+    for (int c0 = cl; c0 < cpr; c0 += kBatch * lpt) {
+      uint4 kr[kBatch], vr[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = c0 + u * lpt;
+        if (c < cpr) {
+          kr[u] = ld_stream(ks + c);
+          vr[u] = ld_stream(vs + c);
+        }
+      }
+      if (slot == -1) continue;
+      if (slot < 0 || slot >= num_slots) {
+        if (c0 == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);
+        continue;
+      }
+      uint4* kd = k_cache + static_cast<int64_t>(slot) * cpr;
+      uint4* vd = v_cache + static_cast<int64_t>(slot) * cpr;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int c = c0 + u * lpt;
+        if (c < cpr) {
+          kd[c] = kr[u];
+          vd[c] = vr[u];
+        }
+      }
     }
-    const int64_t dst = static_cast<int64_t>(slot) * chunks_per_row + chunk;
-    const uint4 kv = ld_stream(k + idx);
-    const uint4 vv = ld_stream(v + idx);
-    k_cache[dst] = kv;
-    v_cache[dst] = vv;
   }
 }
 
@@ -64,15 +93,18 @@ extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v
   pkv::DeviceInfo info;
   if (pkv::device_info(&info) != PKV_OK) return PKV_ECUDA;
 
-  const int32_t chunks_per_row = static_cast<int32_t>(row_bytes / 16);
-  const int64_t total_chunks = static_cast<int64_t>(num_tokens) * chunks_per_row;
+  if (row_bytes / 16 > INT32_MAX) return PKV_EUNSUPPORTED;
+  const int32_t cpr = static_cast<int32_t>(row_bytes / 16);
+  int32_t lpt = 1;
+  while (lpt < cpr && lpt < 32) lpt *= 2;
   const int threads = 256;
-  int64_t blocks = (total_chunks + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(info.sms) * 8;
+  const int64_t tokens_per_block = (threads / 32) * (32 / lpt);
+  int64_t blocks = (num_tokens + tokens_per_block - 1) / tokens_per_block;
+  const int64_t cap = static_cast<int64_t>(info.sms) * kBlocksPerSm;
   if (blocks > cap) blocks = cap;
   kv_store_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, total_chunks, chunks_per_row,
+      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, cpr, lpt,
       static_cast<int64_t>(num_blocks) * block_size, err);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
