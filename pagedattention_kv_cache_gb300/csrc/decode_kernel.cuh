@@ -840,6 +840,11 @@ __global__ void __launch_bounds__(288, 1)
   constexpr int R = G * QL;
   static_assert(R <= 16, "at most 16 rows per KV head");
   constexpr int HH = R <= 8 ? 1 : 2;  // fragment row halves (r0, r0 + 8) that hold query rows
+  // R <= 8: O is accumulated transposed, O^T = V^T P^T, with head_dim in the
+  // M dimension (8 m-tiles of 16) and the rows in N: half the MMAs and half
+  // the accumulator registers of O = P V, whose M rows 8..15 would be empty
+  constexpr bool kT = HH == 1;
+  constexpr int NO = kT ? 8 : 16;
   constexpr float kRescale = 8.0f;
   const int rows_per_seq = QL * p.hq;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -983,6 +988,9 @@ __global__ void __launch_bounds__(288, 1)
   const uint32_t vrow = cbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rs;
   const uint32_t kj = static_cast<uint32_t>(lane >> 3);
   const uint32_t vj = static_cast<uint32_t>(lane >> 4);
+  // transposed P V: matrices 0, 1 read keys 0-7, matrices 2, 3 keys 8-15; odd matrices the upper 8 columns
+  const uint32_t vrowt = cbase + ((lane & 7) + ((lane >> 4) & 1) * 8) * rs;
+  const uint32_t vjt = static_cast<uint32_t>((lane >> 3) & 1);
   // FP8 V: this lane reads 16 codes (chunk lane / 4) of key rows 2c, 2c + 1 and
   // the same + 8; a row's swizzle phase is key & 7
   const uint32_t vq = static_cast<uint32_t>(lane >> 2);
@@ -1037,9 +1045,9 @@ __global__ void __launch_bounds__(288, 1)
     }
     const int lim0 = seg.ctx - QL + (r0 < R ? r0 / G : 0);
     const int lim1 = seg.ctx - QL + (r0 + 8 < R ? (r0 + 8) / G : 0);
-    float o[16][4];
+    float o[NO][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < NO; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
     float m[2] = {-INFINITY, -INFINITY};
@@ -1116,11 +1124,30 @@ __global__ void __launch_bounds__(288, 1)
           mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 1));
           mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 2));
           const float mn = fmaxf(m[hh], mt[hh]);
-          if (mn > m[hh] + kRescale || (m[hh] == -INFINITY && mn != -INFINITY)) {
+          const bool need = mn > m[hh] + kRescale || (m[hh] == -INFINITY && mn != -INFINITY);
+          if constexpr (kT) {
+            // row r0's state lives in quad r0; the accumulators hold rows 2c and 2c + 1
+            if (__any_sync(0xffffffffu, need)) {
+              const float corr = need ? exp2f(m[0] - mn) : 1.f;  // 0 while nothing has been accumulated
+              if (need) {
+                l[0] *= corr;
+                m[0] = mn;
+              }
+              const float c0 = __shfl_sync(0xffffffffu, corr, 8 * c);
+              const float c1 = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
+#pragma unroll
+              for (int j = 0; j < NO; ++j) {
+                o[j][0] *= c0;
+                o[j][2] *= c0;
+                o[j][1] *= c1;
+                o[j][3] *= c1;
+              }
+            }
+          } else if (need) {
             const float corr = exp2f(m[hh] - mn);  // 0 while nothing has been accumulated
             l[hh] *= corr;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < NO; ++j) {
               o[j][2 * hh] *= corr;
               o[j][2 * hh + 1] *= corr;
             }
@@ -1145,7 +1172,9 @@ __global__ void __launch_bounds__(288, 1)
               pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
           }
-          // O += P V: pair keys (2c, 2c+1) and (2c+8, 2c+9) of one column by byte permutes
+          // O^T += V^T P^T: the A fragment pairs keys (2c, 2c+1) and (2c+8, 2c+9)
+          // of one head_dim index by byte permutes of 16 codes of each key row;
+          // m-tile t, row m stands for head_dim 16 m + 2t (m < 8) or 16 (m - 8) + 2t + 1
           const uint4 ra = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a);
           const uint4 rb = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8b);
           const uint4 rc = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a + 8 * rs);
@@ -1153,13 +1182,13 @@ __global__ void __launch_bounds__(288, 1)
           const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
           const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t x01 = pkv::prmt(wa[i], wb[i], 0x5140u), x23 = pkv::prmt(wa[i], wb[i], 0x7362u);
-            const uint32_t y01 = pkv::prmt(wc[i], wd[i], 0x5140u), y23 = pkv::prmt(wc[i], wd[i], 0x7362u);
-            pkv::mma_f16_16816(o[4 * i], pf, pkv::e4m3x2_to_f16x2(x01), pkv::e4m3x2_to_f16x2(y01));
-            pkv::mma_f16_16816(o[4 * i + 1], pf, pkv::e4m3x2_to_f16x2(x01 >> 16), pkv::e4m3x2_to_f16x2(y01 >> 16));
-            pkv::mma_f16_16816(o[4 * i + 2], pf, pkv::e4m3x2_to_f16x2(x23), pkv::e4m3x2_to_f16x2(y23));
-            pkv::mma_f16_16816(o[4 * i + 3], pf, pkv::e4m3x2_to_f16x2(x23 >> 16), pkv::e4m3x2_to_f16x2(y23 >> 16));
+          for (int tm = 0; tm < 8; ++tm) {
+            const uint32_t sel = (tm & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x = pkv::prmt(wa[tm >> 1], wb[tm >> 1], sel);
+            const uint32_t y = pkv::prmt(wc[tm >> 1], wd[tm >> 1], sel);
+            const uint32_t a[4] = {pkv::e4m3x2_to_f16x2(x), pkv::e4m3x2_to_f16x2(x >> 16), pkv::e4m3x2_to_f16x2(y),
+                                   pkv::e4m3x2_to_f16x2(y >> 16)};
+            pkv::mma_f16_16816(o[tm], a, pf[0], pf[2]);
           }
         } else {
 #pragma unroll
@@ -1174,13 +1203,24 @@ __global__ void __launch_bounds__(288, 1)
               pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
           }
-          // O += P V over the 16 keys: 16 n-tiles of 8 columns
+          if constexpr (kT) {
+            // O^T += V^T P^T: m-tile t covers head_dim 16t .. 16t + 15; the four
+            // 8x8 matrices are (keys 0-7 | 8-15) x (head_dim 16t + 0-7 | + 8-15)
 #pragma unroll
-          for (int jp = 0; jp < 8; ++jp) {
-            uint32_t b[4];
-            pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
-            pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
-            pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+            for (int tm = 0; tm < 8; ++tm) {
+              uint32_t a[4];
+              pkv::ldsm_x4_trans(vbase + vrowt + (tm >> 2) * hs + (((2 * (tm & 3) + vjt) ^ xr) << 4), a);
+              pkv::mma_bf16_16816(o[tm], a, pf[0], pf[2]);
+            }
+          } else {
+            // O += P V over the 16 keys: 16 n-tiles of 8 columns
+#pragma unroll
+            for (int jp = 0; jp < 8; ++jp) {
+              uint32_t b[4];
+              pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
+              pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
+              pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+            }
           }
         }
       }
@@ -1194,104 +1234,215 @@ __global__ void __launch_bounds__(288, 1)
       l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
     }
 
-    // merge the warps that share KV head g (token phases)
-    if (p.wph > 1) {
-      const int rec = D + 2;
+    if constexpr (kT) {
+      // this lane's accumulators hold rows 2c and 2c + 1 (columns of O^T); their
+      // (m, l) come from the quads that own those rows.  Accumulator (tm, e)
+      // is head_dim index dA(tm) (e < 2) or dA(tm) + dB (e >= 2).
+      const float mr0 = __shfl_sync(0xffffffffu, m[0], 8 * c), mr1 = __shfl_sync(0xffffffffu, m[0], 8 * c + 4);
+      const float lr0 = __shfl_sync(0xffffffffu, l[0], 8 * c), lr1 = __shfl_sync(0xffffffffu, l[0], 8 * c + 4);
+      float mr[2] = {mr0, mr1}, lr[2] = {lr0, lr1};
+      const int q4 = lane >> 2;
+      constexpr int dB = kFp8 ? 1 : 8;
+      auto dA = [&](int tm) { return kFp8 ? 16 * q4 + 2 * tm : 16 * tm + q4; };
+      if (p.wph > 1) {
+        const int rec = D + 2;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int rho = r0 + 8 * hh;
-        if (rho < R) {
-          float* dstm = merge + (static_cast<size_t>(warp) * R + rho) * rec;
+        for (int i = 0; i < 2; ++i) {
+          const int row = 2 * c + i;
+          if (row < R) {
+            float* dstm = merge + (static_cast<size_t>(warp) * R + row) * rec;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float2*>(dstm + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
-          if (c == 0) {
-            dstm[D] = m[hh];
-            dstm[D + 1] = l[hh];
+            for (int tm = 0; tm < NO; ++tm) {
+              dstm[dA(tm)] = o[tm][i];
+              dstm[dA(tm) + dB] = o[tm][2 + i];
+            }
+          }
+        }
+        if (c == 0 && r0 < R) {
+          float* dstm = merge + (static_cast<size_t>(warp) * R + r0) * rec;
+          dstm[D] = m[0];
+          dstm[D + 1] = l[0];
+        }
+        pkv::named_barrier_sync(1, nthreads_c);
+        if (phase == 0) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int row = 2 * c + i;
+            if (row >= R) continue;
+            float mm = mr[i];
+            for (int ph = 1; ph < p.wph; ++ph)
+              mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + row) * rec + D]);
+            const float w0 = mm == -INFINITY ? 0.f : exp2f(mr[i] - mm);
+            float ll = lr[i] * w0;
+#pragma unroll
+            for (int tm = 0; tm < NO; ++tm) {
+              o[tm][i] *= w0;
+              o[tm][2 + i] *= w0;
+            }
+            for (int ph = 1; ph < p.wph; ++ph) {
+              const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + row) * rec;
+              const float w = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mm);
+              ll += w * src[D + 1];
+#pragma unroll
+              for (int tm = 0; tm < NO; ++tm) {
+                o[tm][i] += w * src[dA(tm)];
+                o[tm][2 + i] += w * src[dA(tm) + dB];
+              }
+            }
+            mr[i] = mm;
+            lr[i] = ll;
+          }
+        }
+        pkv::named_barrier_sync(1, nthreads_c);
+      }
+      // write the result (whole sequence) or this part's state; for an FP8
+      // cache V's scale comes off here (P's 2^7 cancels against l)
+      if (phase == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int row = 2 * c + i;
+          if (row >= R) continue;
+          const int head = (row / G) * p.hq + g * G + row % G;
+          const float vs = kFp8 ? p.v_scale : 1.f;
+          if (seg.nparts == 1) {
+            const float ws = vs / lr[i];
+            T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(seg.b) * rows_per_seq + head) * D;
+            if constexpr (kFp8) {
+              // this lane's 16 outputs are contiguous: head_dim 16 q4 .. 16 q4 + 15
+              uint32_t w[8];
+#pragma unroll
+              for (int tm = 0; tm < 8; ++tm) w[tm] = pkv::pack_bf16x2(o[tm][i] * ws, o[tm][2 + i] * ws);
+              uint4* dst = reinterpret_cast<uint4*>(orow + 16 * q4);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+              for (int tm = 0; tm < NO; ++tm) {
+                orow[dA(tm)] = static_cast<T>(o[tm][i] * ws);
+                orow[dA(tm) + dB] = static_cast<T>(o[tm][2 + i] * ws);
+              }
+            }
+          } else {
+            float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
+            if constexpr (kFp8) {
+              float4* dst = reinterpret_cast<float4*>(po + 16 * q4);
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                dst[u] = make_float4(o[2 * u][i] * vs, o[2 * u][2 + i] * vs, o[2 * u + 1][i] * vs,
+                                     o[2 * u + 1][2 + i] * vs);
+            } else {
+#pragma unroll
+              for (int tm = 0; tm < NO; ++tm) {
+                po[dA(tm)] = o[tm][i];
+                po[dA(tm) + dB] = o[tm][2 + i];
+              }
+            }
+            if (q4 == 0)
+              *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
+                  make_float2(mr[i], lr[i]);
           }
         }
       }
-      pkv::named_barrier_sync(1, nthreads_c);
+    } else {
+      // merge the warps that share KV head g (token phases)
+      if (p.wph > 1) {
+        const int rec = D + 2;
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rho = r0 + 8 * hh;
+          if (rho < R) {
+            float* dstm = merge + (static_cast<size_t>(warp) * R + rho) * rec;
+  #pragma unroll
+            for (int j = 0; j < 16; ++j)
+              *reinterpret_cast<float2*>(dstm + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
+            if (c == 0) {
+              dstm[D] = m[hh];
+              dstm[D + 1] = l[hh];
+            }
+          }
+        }
+        pkv::named_barrier_sync(1, nthreads_c);
+        if (phase == 0) {
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int rho = r0 + 8 * hh;
+            if (rho >= R) continue;
+            float mm = m[hh];
+            for (int ph = 1; ph < p.wph; ++ph)
+              mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec + D]);
+            const float w0 = mm == -INFINITY ? 0.f : exp2f(m[hh] - mm);
+            float ll = l[hh] * w0;
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              o[j][2 * hh] *= w0;
+              o[j][2 * hh + 1] *= w0;
+            }
+            for (int ph = 1; ph < p.wph; ++ph) {
+              const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec;
+              const float w = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mm);
+              ll += w * src[D + 1];
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float2 v = *reinterpret_cast<const float2*>(src + j * 8 + 2 * c);
+                o[j][2 * hh] += w * v.x;
+                o[j][2 * hh + 1] += w * v.y;
+              }
+            }
+            m[hh] = mm;
+            l[hh] = ll;
+          }
+        }
+        pkv::named_barrier_sync(1, nthreads_c);
+      }
+
+      // write the result (whole sequence) or this part's state
       if (phase == 0) {
-#pragma unroll
+  #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int rho = r0 + 8 * hh;
           if (rho >= R) continue;
-          float mm = m[hh];
-          for (int ph = 1; ph < p.wph; ++ph)
-            mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec + D]);
-          const float w0 = mm == -INFINITY ? 0.f : exp2f(m[hh] - mm);
-          float ll = l[hh] * w0;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            o[j][2 * hh] *= w0;
-            o[j][2 * hh + 1] *= w0;
-          }
-          for (int ph = 1; ph < p.wph; ++ph) {
-            const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec;
-            const float w = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mm);
-            ll += w * src[D + 1];
-#pragma unroll
+          const int head = (rho / G) * p.hq + g * G + rho % G;
+          if constexpr (kFp8) {
+            // accumulator (j, 2c + e) is output 32c + 16e + j; V's scale comes off here
+            // (P's 2^7 cancels against l)
+            const float ws = seg.nparts == 1 ? p.v_scale / l[hh] : p.v_scale;
+            float f[32];
+  #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float2 v = *reinterpret_cast<const float2*>(src + j * 8 + 2 * c);
-              o[j][2 * hh] += w * v.x;
-              o[j][2 * hh + 1] += w * v.y;
+              f[j] = o[j][2 * hh] * ws;
+              f[16 + j] = o[j][2 * hh + 1] * ws;
             }
-          }
-          m[hh] = mm;
-          l[hh] = ll;
-        }
-      }
-      pkv::named_barrier_sync(1, nthreads_c);
-    }
-
-    // write the result (whole sequence) or this part's state
-    if (phase == 0) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int rho = r0 + 8 * hh;
-        if (rho >= R) continue;
-        const int head = (rho / G) * p.hq + g * G + rho % G;
-        if constexpr (kFp8) {
-          // accumulator (j, 2c + e) is output 32c + 16e + j; V's scale comes off here
-          // (P's 2^7 cancels against l)
-          const float ws = seg.nparts == 1 ? p.v_scale / l[hh] : p.v_scale;
-          float f[32];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            f[j] = o[j][2 * hh] * ws;
-            f[16 + j] = o[j][2 * hh + 1] * ws;
-          }
-          if (seg.nparts == 1) {
-            uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                   (static_cast<size_t>(seg.b) * rows_per_seq + head) * D + 32 * c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              orow[u] = make_uint4(pkv::pack_bf16x2(f[8 * u], f[8 * u + 1]), pkv::pack_bf16x2(f[8 * u + 2], f[8 * u + 3]),
-                                   pkv::pack_bf16x2(f[8 * u + 4], f[8 * u + 5]),
-                                   pkv::pack_bf16x2(f[8 * u + 6], f[8 * u + 7]));
+            if (seg.nparts == 1) {
+              uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
+                                                     (static_cast<size_t>(seg.b) * rows_per_seq + head) * D + 32 * c);
+  #pragma unroll
+              for (int u = 0; u < 4; ++u)
+                orow[u] = make_uint4(pkv::pack_bf16x2(f[8 * u], f[8 * u + 1]), pkv::pack_bf16x2(f[8 * u + 2], f[8 * u + 3]),
+                                     pkv::pack_bf16x2(f[8 * u + 4], f[8 * u + 5]),
+                                     pkv::pack_bf16x2(f[8 * u + 6], f[8 * u + 7]));
+            } else {
+              float4* po = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D +
+                                                     32 * c);
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) po[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
+            }
+          } else if (seg.nparts == 1) {
+            const float inv = 1.f / l[hh];
+            uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
+                                                         (static_cast<size_t>(seg.b) * rows_per_seq + head) * D);
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) orow[j * 4 + c] = pkv::pack_bf16x2(o[j][2 * hh] * inv, o[j][2 * hh + 1] * inv);
           } else {
-            float4* po = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D +
-                                                   32 * c);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) po[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
+            float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
+  #pragma unroll
+            for (int j = 0; j < 16; ++j)
+              *reinterpret_cast<float2*>(po + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
           }
-        } else if (seg.nparts == 1) {
-          const float inv = 1.f / l[hh];
-          uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
-                                                       (static_cast<size_t>(seg.b) * rows_per_seq + head) * D);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) orow[j * 4 + c] = pkv::pack_bf16x2(o[j][2 * hh] * inv, o[j][2 * hh + 1] * inv);
-        } else {
-          float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float2*>(po + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
-        }
-        if (seg.nparts > 1) {
-          if (c == 0)
-            *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
-                make_float2(m[hh], l[hh]);
+          if (seg.nparts > 1) {
+            if (c == 0)
+              *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * 2) =
+                  make_float2(m[hh], l[hh]);
+          }
         }
       }
     }
