@@ -720,7 +720,8 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
 #pragma unroll
         for (int h = 0; h < R; ++h) {
           float mm = m[h];
-          for (int ph = 1; ph < p.wph; ++ph) mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + h) * rec + D]);
+          for (int ph = 1; ph < p.wph; ++ph)
+            mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + h) * rec + D]);
           const float w0 = mm == -INFINITY ? 0.f : exp2f(m[h] - mm);
           float ll = l[h] * w0;
 #pragma unroll
@@ -828,6 +829,14 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
 //    four key rows and byte-permutes key pairs together; n-tile j, column n
 //    then stands for head_dim index 16 n + j, and a lane's accumulators cover
 //    32 consecutive outputs.
+// 16-key chunks a consumer warp takes per stage: two for an FP8 cache (its
+// stages hold twice the tokens in the same bytes, and the second chunk's
+// scores overlap the first's latency), one for bf16.
+template <typename TC>
+__host__ __device__ constexpr int mma_chunks_per_warp() {
+  return std::is_same<TC, __nv_fp8_e4m3>::value ? 2 : 1;
+}
+
 template <int G, int QL, typename TC = __nv_bfloat16>
 __global__ void __launch_bounds__(288, 1)
     paged_decode_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
@@ -836,6 +845,7 @@ __global__ void __launch_bounds__(288, 1)
   constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
   constexpr int ES = static_cast<int>(sizeof(TC));  // bytes per cache element
   constexpr int NH = ES;                             // tensor copies per K (or V) box: 128-byte rows
+  constexpr int NSUB = mma_chunks_per_warp<TC>();
   constexpr int D = 128;
   constexpr int R = G * QL;
   static_assert(R <= 16, "at most 16 rows per KV head");
@@ -904,7 +914,7 @@ __global__ void __launch_bounds__(288, 1)
           const int s = it % p.stages;
           const uint32_t use = it / p.stages;
           const int tc = t + lane * kMmaTokens;
-          const bool mine = lane < p.wph && tc < seg.t1;
+          const bool mine = lane < p.t_stage / kMmaTokens && tc < seg.t1;
           const int blk = tc / p.block_size;
           const int phys = mine ? __ldg(table + blk) : 0;
           if (lane == 0 && use > 0) wait_or_abort(&empty[s], (use & 1u) ^ 1u, abort_flag, p.err);
@@ -983,7 +993,8 @@ __global__ void __launch_bounds__(288, 1)
   const int hs = p.tma ? box_bytes : 128;
   const uint32_t xr = p.tma ? static_cast<uint32_t>(lane & 7) : 0u;
   // chunk base (K) of this warp in stage 0, relative to the stage
-  const int cbase = p.tma ? phase * NH * box_bytes + g * kMmaTokens * 128 : phase * kMmaTokens * ts + g * D * ES;
+  const int csub = p.tma ? NH * box_bytes : kMmaTokens * ts;  // bytes from one 16-token chunk to the next
+  const int cbase = phase * NSUB * csub + (p.tma ? g * kMmaTokens * 128 : g * D * ES);
   const uint32_t krow = cbase + (lane & 7) * rs;
   const uint32_t vrow = cbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * rs;
   const uint32_t kj = static_cast<uint32_t>(lane >> 3);
@@ -1043,6 +1054,19 @@ __global__ void __launch_bounds__(288, 1)
         }
       }
     }
+    // the A fragment of k16 step kk; with R <= 8 its rows r0 + 8 are zero
+    // constants, so their registers are not kept
+    struct QFrag {
+      uint32_t r[4];
+    };
+    auto qa = [&](int kk) {
+      QFrag f;
+      f.r[0] = qf[kk][0];
+      f.r[1] = kT ? 0u : qf[kk][1];
+      f.r[2] = qf[kk][2];
+      f.r[3] = kT ? 0u : qf[kk][3];
+      return f;
+    };
     const int lim0 = seg.ctx - QL + (r0 < R ? r0 / G : 0);
     const int lim1 = seg.ctx - QL + (r0 + 8 < R ? (r0 + 8) / G : 0);
     float o[NO][4];
@@ -1058,67 +1082,73 @@ __global__ void __launch_bounds__(288, 1)
       const uint32_t use = it / p.stages;
       wait_or_abort(&full[s], use & 1u, abort_flag, p.err);
       const int nt = min(p.t_stage, seg.t1 - t);
-      const int tt0 = phase * kMmaTokens;
-      const int nv = min(max(nt - tt0, 0), kMmaTokens);  // valid keys of this warp's chunk
-      if (nv > 0) {
-        const uint32_t kbase = stage_addr + s * p.stage_bytes;
-        const uint32_t vbase = kbase + p.stage_bytes / 2;
-        if (nv < kMmaTokens) {
-          // V rows past the last key hold stale bytes: zero them so 0 * stale never reaches O
-          constexpr int CPR = 8 * NH;  // 16-byte chunks of one head's row
-          unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + cbase;
-          for (int idx = lane; idx < (kMmaTokens - nv) * CPR; idx += 32)
-            *reinterpret_cast<uint4*>(vrows + (nv + idx / CPR) * rs + ((idx % CPR) / 8) * hs + (idx % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-        }
-        // S = Q K^T for 16 keys (two n-tiles of 8)
-        float sacc[2][4];
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[nb][e] = 0.f;
-        if constexpr (kFp8) {
-          // a word of four codes widens to the B pairs of one k16 step
-#pragma unroll
-          for (int q4 = 0; q4 < 2; ++q4) {
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-              uint32_t b[4];
-              pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (((q4 * 4 + kj) ^ xr) << 4), b);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                pkv::mma_f16_16816(sacc[nb], qf[4 * q4 + i], pkv::e4m3x2_to_f16x2(b[i]),
-                                   pkv::e4m3x2_to_f16x2(b[i] >> 16));
-            }
-          }
-        } else {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-              uint32_t b[4];
-              pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (k4 >> 1) * hs + ((((k4 & 1) * 4 + kj) ^ xr) << 4), b);
-              pkv::mma_bf16_16816(sacc[nb], qf[2 * k4], b[0], b[1]);
-              pkv::mma_bf16_16816(sacc[nb], qf[2 * k4 + 1], b[2], b[3]);
-            }
-          }
-        }
-        // scale, mask, online softmax per row (lazy rescale of O); with R <= 8
-        // the fragment rows r0 + 8 hold no query row and are skipped (P = 0)
+      // this warp's NSUB chunks of 16 keys are chunks phase * NSUB + sub of the stage;
+      // their scores share one running maximum, so the rescale check runs once
+      const int tw0 = phase * NSUB * kMmaTokens;
+      if (nt > tw0) {
+        float sacc[NSUB][2][4];
         float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
+        for (int sub = 0; sub < NSUB; ++sub) {
+          const int tt0 = tw0 + sub * kMmaTokens;
+          const int nv = min(max(nt - tt0, 0), kMmaTokens);  // valid keys of this chunk
 #pragma unroll
-          for (int e = 0; e < 2 * HH; ++e) {
-            const int key = nb * 8 + 2 * c + (e & 1);
-            float x = sacc[nb][e] * qmul[e >> 1];
-            const bool visible = key < nv && (QL == 1 || t + tt0 + key <= ((e < 2) ? lim0 : lim1));
-            x = visible ? x : -INFINITY;
-            sacc[nb][e] = x;
-            mt[e >> 1] = fmaxf(mt[e >> 1], x);
+          for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[sub][nb][e] = nv > 0 ? 0.f : -INFINITY;
+          if (nv == 0) continue;  // only a later chunk can be empty; its P is 0
+          const uint32_t kbase = stage_addr + s * p.stage_bytes + sub * csub;
+          if (nv < kMmaTokens) {
+            // V rows past the last key hold stale bytes: zero them so 0 * stale never reaches O
+            constexpr int CPR = 8 * NH;  // 16-byte chunks of one head's row
+            unsigned char* vrows = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub + cbase;
+            for (int idx = lane; idx < (kMmaTokens - nv) * CPR; idx += 32)
+              *reinterpret_cast<uint4*>(vrows + (nv + idx / CPR) * rs + ((idx % CPR) / 8) * hs + (idx % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
           }
+          // S = Q K^T for 16 keys (two n-tiles of 8)
+          if constexpr (kFp8) {
+            // a word of four codes widens to the B pairs of one k16 step
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {
+#pragma unroll
+              for (int nb = 0; nb < 2; ++nb) {
+                uint32_t b[4];
+                pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (((q4 * 4 + kj) ^ xr) << 4), b);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  pkv::mma_f16_16816(sacc[sub][nb], qa(4 * q4 + i).r, pkv::e4m3x2_to_f16x2(b[i]),
+                                     pkv::e4m3x2_to_f16x2(b[i] >> 16));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+              for (int nb = 0; nb < 2; ++nb) {
+                uint32_t b[4];
+                pkv::ldsm_x4(kbase + krow + nb * 8 * rs + (k4 >> 1) * hs + ((((k4 & 1) * 4 + kj) ^ xr) << 4), b);
+                pkv::mma_bf16_16816(sacc[sub][nb], qa(2 * k4).r, b[0], b[1]);
+                pkv::mma_bf16_16816(sacc[sub][nb], qa(2 * k4 + 1).r, b[2], b[3]);
+              }
+            }
+          }
+          // scale, mask; with R <= 8 the fragment rows r0 + 8 hold no query row and are skipped (P = 0)
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2 * HH; ++e) {
+              const int key = nb * 8 + 2 * c + (e & 1);
+              float x = sacc[sub][nb][e] * qmul[e >> 1];
+              const bool visible = key < nv && (QL == 1 || t + tt0 + key <= ((e < 2) ? lim0 : lim1));
+              x = visible ? x : -INFINITY;
+              sacc[sub][nb][e] = x;
+              mt[e >> 1] = fmaxf(mt[e >> 1], x);
+            }
+        }
+        // online softmax per row (lazy rescale of O)
 #pragma unroll
         for (int hh = 0; hh < HH; ++hh) {
           mt[hh] = fmaxf(mt[hh], __shfl_xor_sync(0xffffffffu, mt[hh], 1));
@@ -1156,70 +1186,81 @@ __global__ void __launch_bounds__(288, 1)
         }
         const float mu0 = m[0] == -INFINITY ? 0.f : m[0];
         const float mu1 = m[1] == -INFINITY ? 0.f : m[1];
-        uint32_t pf[4];
-        if constexpr (kFp8) {
-          // P as f16 times 2^7; l sums the same rounded weights
-          constexpr float kPs = 128.0f;
 #pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            const __half2 lo = __floats2half2_rn(exp2f(sacc[nb][0] - mu0) * kPs, exp2f(sacc[nb][1] - mu0) * kPs);
-            l[0] += __low2float(lo) + __high2float(lo);
-            pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
-            pf[2 * nb + 1] = 0u;
-            if constexpr (HH == 2) {
-              const __half2 hi = __floats2half2_rn(exp2f(sacc[nb][2] - mu1) * kPs, exp2f(sacc[nb][3] - mu1) * kPs);
-              l[1] += __low2float(hi) + __high2float(hi);
-              pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        for (int sub = 0; sub < NSUB; ++sub) {
+          if (nt <= tw0 + sub * kMmaTokens) continue;
+          const uint32_t vbase = stage_addr + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub;
+          const unsigned char* vstage = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub;
+          (void)vstage;
+          uint32_t pf[4];
+          if constexpr (kFp8) {
+            // P as f16 times 2^7; l sums the same rounded weights
+            constexpr float kPs = 128.0f;
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+              const __half2 lo =
+                  __floats2half2_rn(exp2f(sacc[sub][nb][0] - mu0) * kPs, exp2f(sacc[sub][nb][1] - mu0) * kPs);
+              l[0] += __low2float(lo) + __high2float(lo);
+              pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
+              pf[2 * nb + 1] = 0u;
+              if constexpr (HH == 2) {
+                const __half2 hi =
+                    __floats2half2_rn(exp2f(sacc[sub][nb][2] - mu1) * kPs, exp2f(sacc[sub][nb][3] - mu1) * kPs);
+                l[1] += __low2float(hi) + __high2float(hi);
+                pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+              }
             }
-          }
-          // O^T += V^T P^T: the A fragment pairs keys (2c, 2c+1) and (2c+8, 2c+9)
-          // of one head_dim index by byte permutes of 16 codes of each key row;
-          // m-tile t, row m stands for head_dim 16 m + 2t (m < 8) or 16 (m - 8) + 2t + 1
-          const uint4 ra = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a);
-          const uint4 rb = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8b);
-          const uint4 rc = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8a + 8 * rs);
-          const uint4 rd = pkv::lds128(stage_base + s * p.stage_bytes + p.stage_bytes / 2 + v8b + 8 * rs);
-          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-          const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
-#pragma unroll
-          for (int tm = 0; tm < 8; ++tm) {
-            const uint32_t sel = (tm & 1) ? 0x7362u : 0x5140u;
-            const uint32_t x = pkv::prmt(wa[tm >> 1], wb[tm >> 1], sel);
-            const uint32_t y = pkv::prmt(wc[tm >> 1], wd[tm >> 1], sel);
-            const uint32_t a[4] = {pkv::e4m3x2_to_f16x2(x), pkv::e4m3x2_to_f16x2(x >> 16), pkv::e4m3x2_to_f16x2(y),
-                                   pkv::e4m3x2_to_f16x2(y >> 16)};
-            pkv::mma_f16_16816(o[tm], a, pf[0], pf[2]);
-          }
-        } else {
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(exp2f(sacc[nb][0] - mu0), exp2f(sacc[nb][1] - mu0));
-            l[0] += __low2float(lo) + __high2float(lo);
-            pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
-            pf[2 * nb + 1] = 0u;
-            if constexpr (HH == 2) {
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(exp2f(sacc[nb][2] - mu1), exp2f(sacc[nb][3] - mu1));
-              l[1] += __low2float(hi) + __high2float(hi);
-              pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-            }
-          }
-          if constexpr (kT) {
-            // O^T += V^T P^T: m-tile t covers head_dim 16t .. 16t + 15; the four
-            // 8x8 matrices are (keys 0-7 | 8-15) x (head_dim 16t + 0-7 | + 8-15)
+            // O^T += V^T P^T: the A fragment pairs keys (2c, 2c+1) and (2c+8, 2c+9)
+            // of one head_dim index by byte permutes of 16 codes of each key row;
+            // m-tile t, row m stands for head_dim 16 m + 2t (m < 8) or 16 (m - 8) + 2t + 1
+            const uint4 ra = pkv::lds128(vstage + v8a);
+            const uint4 rb = pkv::lds128(vstage + v8b);
+            const uint4 rc = pkv::lds128(vstage + v8a + 8 * rs);
+            const uint4 rd = pkv::lds128(vstage + v8b + 8 * rs);
+            const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+            const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
 #pragma unroll
             for (int tm = 0; tm < 8; ++tm) {
-              uint32_t a[4];
-              pkv::ldsm_x4_trans(vbase + vrowt + (tm >> 2) * hs + (((2 * (tm & 3) + vjt) ^ xr) << 4), a);
-              pkv::mma_bf16_16816(o[tm], a, pf[0], pf[2]);
+              const uint32_t sel = (tm & 1) ? 0x7362u : 0x5140u;
+              const uint32_t x = pkv::prmt(wa[tm >> 1], wb[tm >> 1], sel);
+              const uint32_t y = pkv::prmt(wc[tm >> 1], wd[tm >> 1], sel);
+              const uint32_t a[4] = {pkv::e4m3x2_to_f16x2(x), pkv::e4m3x2_to_f16x2(x >> 16), pkv::e4m3x2_to_f16x2(y),
+                                     pkv::e4m3x2_to_f16x2(y >> 16)};
+              pkv::mma_f16_16816(o[tm], a, pf[0], pf[2]);
             }
           } else {
-            // O += P V over the 16 keys: 16 n-tiles of 8 columns
 #pragma unroll
-            for (int jp = 0; jp < 8; ++jp) {
-              uint32_t b[4];
-              pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
-              pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
-              pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+            for (int nb = 0; nb < 2; ++nb) {
+              const __nv_bfloat162 lo =
+                  __floats2bfloat162_rn(exp2f(sacc[sub][nb][0] - mu0), exp2f(sacc[sub][nb][1] - mu0));
+              l[0] += __low2float(lo) + __high2float(lo);
+              pf[2 * nb] = *reinterpret_cast<const uint32_t*>(&lo);
+              pf[2 * nb + 1] = 0u;
+              if constexpr (HH == 2) {
+                const __nv_bfloat162 hi =
+                    __floats2bfloat162_rn(exp2f(sacc[sub][nb][2] - mu1), exp2f(sacc[sub][nb][3] - mu1));
+                l[1] += __low2float(hi) + __high2float(hi);
+                pf[2 * nb + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+              }
+            }
+            if constexpr (kT) {
+              // O^T += V^T P^T: m-tile t covers head_dim 16t .. 16t + 15; the four
+              // 8x8 matrices are (keys 0-7 | 8-15) x (head_dim 16t + 0-7 | + 8-15)
+#pragma unroll
+              for (int tm = 0; tm < 8; ++tm) {
+                uint32_t a[4];
+                pkv::ldsm_x4_trans(vbase + vrowt + (tm >> 2) * hs + (((2 * (tm & 3) + vjt) ^ xr) << 4), a);
+                pkv::mma_bf16_16816(o[tm], a, pf[0], pf[2]);
+              }
+            } else {
+              // O += P V over the 16 keys: 16 n-tiles of 8 columns
+#pragma unroll
+              for (int jp = 0; jp < 8; ++jp) {
+                uint32_t b[4];
+                pkv::ldsm_x4_trans(vbase + vrow + (jp >> 2) * hs + (((2 * (jp & 3) + vj) ^ xr) << 4), b);
+                pkv::mma_bf16_16816(o[2 * jp], pf, b[0], b[1]);
+                pkv::mma_bf16_16816(o[2 * jp + 1], pf, b[2], b[3]);
+              }
             }
           }
         }
@@ -1227,7 +1268,6 @@ __global__ void __launch_bounds__(288, 1)
       __syncwarp();
       if (lane == 0) pkv::mbar_arrive(&empty[s]);
     }
-
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
@@ -1347,12 +1387,12 @@ __global__ void __launch_bounds__(288, 1)
       // merge the warps that share KV head g (token phases)
       if (p.wph > 1) {
         const int rec = D + 2;
-  #pragma unroll
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int rho = r0 + 8 * hh;
           if (rho < R) {
             float* dstm = merge + (static_cast<size_t>(warp) * R + rho) * rec;
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 16; ++j)
               *reinterpret_cast<float2*>(dstm + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
             if (c == 0) {
@@ -1363,7 +1403,7 @@ __global__ void __launch_bounds__(288, 1)
         }
         pkv::named_barrier_sync(1, nthreads_c);
         if (phase == 0) {
-  #pragma unroll
+#pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int rho = r0 + 8 * hh;
             if (rho >= R) continue;
@@ -1372,7 +1412,7 @@ __global__ void __launch_bounds__(288, 1)
               mm = fmaxf(mm, merge[(static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec + D]);
             const float w0 = mm == -INFINITY ? 0.f : exp2f(m[hh] - mm);
             float ll = l[hh] * w0;
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 16; ++j) {
               o[j][2 * hh] *= w0;
               o[j][2 * hh + 1] *= w0;
@@ -1381,7 +1421,7 @@ __global__ void __launch_bounds__(288, 1)
               const float* src = merge + (static_cast<size_t>(ph * p.hkv + g) * R + rho) * rec;
               const float w = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mm);
               ll += w * src[D + 1];
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float2 v = *reinterpret_cast<const float2*>(src + j * 8 + 2 * c);
                 o[j][2 * hh] += w * v.x;
@@ -1397,44 +1437,20 @@ __global__ void __launch_bounds__(288, 1)
 
       // write the result (whole sequence) or this part's state
       if (phase == 0) {
-  #pragma unroll
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int rho = r0 + 8 * hh;
           if (rho >= R) continue;
           const int head = (rho / G) * p.hq + g * G + rho % G;
-          if constexpr (kFp8) {
-            // accumulator (j, 2c + e) is output 32c + 16e + j; V's scale comes off here
-            // (P's 2^7 cancels against l)
-            const float ws = seg.nparts == 1 ? p.v_scale / l[hh] : p.v_scale;
-            float f[32];
-  #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              f[j] = o[j][2 * hh] * ws;
-              f[16 + j] = o[j][2 * hh + 1] * ws;
-            }
-            if (seg.nparts == 1) {
-              uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                     (static_cast<size_t>(seg.b) * rows_per_seq + head) * D + 32 * c);
-  #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                orow[u] = make_uint4(pkv::pack_bf16x2(f[8 * u], f[8 * u + 1]), pkv::pack_bf16x2(f[8 * u + 2], f[8 * u + 3]),
-                                     pkv::pack_bf16x2(f[8 * u + 4], f[8 * u + 5]),
-                                     pkv::pack_bf16x2(f[8 * u + 6], f[8 * u + 7]));
-            } else {
-              float4* po = reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D +
-                                                     32 * c);
-  #pragma unroll
-              for (int u = 0; u < 8; ++u) po[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
-            }
-          } else if (seg.nparts == 1) {
+          if (seg.nparts == 1) {
             const float inv = 1.f / l[hh];
             uint32_t* orow = reinterpret_cast<uint32_t*>(static_cast<T*>(p.out) +
                                                          (static_cast<size_t>(seg.b) * rows_per_seq + head) * D);
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 16; ++j) orow[j * 4 + c] = pkv::pack_bf16x2(o[j][2 * hh] * inv, o[j][2 * hh + 1] * inv);
           } else {
             float* po = p.part_o + (static_cast<size_t>(seg.slot) * rows_per_seq + head) * D;
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 16; ++j)
               *reinterpret_cast<float2*>(po + j * 8 + 2 * c) = make_float2(o[j][2 * hh], o[j][2 * hh + 1]);
           }
@@ -1521,7 +1537,7 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   LaunchShape ls;
   ls.wph = p.hkv >= 8 ? 1 : 8 / p.hkv;
   ls.nw = p.hkv * ls.wph;
-  ls.t_stage = kMmaTokens * ls.wph;
+  ls.t_stage = kMmaTokens * mma_chunks_per_warp<TC>() * ls.wph;
   // tensor-copy layout when every 16-token box lies in one block
   alignas(64) CUtensorMap maps[2];
   std::memset(maps, 0, sizeof(maps));
