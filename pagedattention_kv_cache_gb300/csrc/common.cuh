@@ -223,28 +223,4 @@ struct Chunk<float> {
   }
 };
 
-// 16 FP8 E4M3 codes, widened exactly (E4M3 -> f16 -> f32).  Codes are read
-// as data, so NaN codes (0x7F, 0xFF) come out as NaN.
-template <>
-struct Chunk<__nv_fp8_e4m3> {
-  static constexpr int N = 16;
-  __device__ __forceinline__ static void unpack(const uint4& c, float* f) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t h01, h23;
-      const uint16_t lo = static_cast<uint16_t>(w[i] & 0xffffu);
-      const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(lo));
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hi));
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-      f[4 * i] = a.x;
-      f[4 * i + 1] = a.y;
-      f[4 * i + 2] = b.x;
-      f[4 * i + 3] = b.y;
-    }
-  }
-};
-
 }  // namespace pkv

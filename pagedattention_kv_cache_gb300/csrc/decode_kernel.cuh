@@ -66,44 +66,6 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// d0 += a.lo * b.lo and d1 += a.hi * b.hi, a and b f16 pairs, fp32 sums: the
-// mixed-precision fma of the sm_100 family multiplies the f16 operands exactly
-// and rounds once into fp32, so no f16 -> f32 conversion is issued.
-__device__ __forceinline__ void fma_h2(float& d0, float& d1, uint32_t a, uint32_t b) {
-  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-      "mov.b32 {a0, a1}, %2;\n\t"
-      "mov.b32 {b0, b1}, %3;\n\t"
-      "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
-      "fma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "r"(a), "r"(b));
-}
-
-// d0 += p * v.lo and d1 += p * v.hi (p one f16, v an f16 pair), fp32 sums.
-__device__ __forceinline__ void fma_h1(float& d0, float& d1, uint16_t p, uint32_t v) {
-  asm("{\n\t.reg .f16 v0, v1;\n\t"
-      "mov.b32 {v0, v1}, %2;\n\t"
-      "fma.rn.f32.f16 %0, %3, v0, %0;\n\t"
-      "fma.rn.f32.f16 %1, %3, v1, %1;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "r"(v), "h"(p));
-}
-
-// Sixteen E4M3 codes to eight f16 pairs (exact: every E4M3 value is an f16).
-__device__ __forceinline__ void e4m3x16_to_f16x2(const uint4& c, uint32_t* h) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i]) : "h"(static_cast<uint16_t>(w[i] & 0xffffu)));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i + 1]) : "h"(static_cast<uint16_t>(w[i] >> 16)));
-  }
-}
-
-// P of an FP8-cache stage is carried as f16 scaled by 2^15 (P <= 1, so no
-// overflow, and weights down to 2^-39 stay representable); the factor comes
-// off with V's scale at the end.
-constexpr float kFp8PScale = 32768.0f;
-
 // Register shape of a consumer warp that holds R query rows (query heads x
 // query tokens) of one KV head.
 template <typename T, int D, int R>
@@ -116,14 +78,9 @@ struct Shape {
   static constexpr int CPL = CHUNKS / LPT;                  // chunks per lane
   static constexpr int EPL = CPL * EPC;                     // elements per lane
   static constexpr int TPW = 32 / LPT;                      // tokens per warp round
-  // CTAs per SM: an FP8 cache with R <= 2 runs two (the per-byte work is
-  // twice bf16's, and the extra warps hide its latency), everything else one
-  static constexpr int CTAS = (sizeof(T) == 1 && R <= 2) ? 2 : 1;
   // rounds per stage per warp: short rows (bf16 with head_dim 64) take more
-  // tokens per stage so a stage still moves a useful number of bytes; an FP8
-  // stage stays at four rounds to fit two CTAs' rings in shared memory
-  static constexpr int ROUNDS =
-      (ROW_BYTES >= 512 || R >= 5) ? 2 : ((ROW_BYTES <= 128 && R <= 2 && CTAS == 1) ? 8 : 4);
+  // tokens per stage so a stage still moves a useful number of bytes
+  static constexpr int ROUNDS = (ROW_BYTES >= 512 || R >= 5) ? 2 : ((ROW_BYTES <= 128 && R <= 2) ? 8 : 4);
   static_assert(CPL >= 1, "head row too short for the lane split");
 };
 
@@ -416,13 +373,13 @@ __device__ __forceinline__ void combine_if_last(const Params& p, const Segment& 
 
 // G query heads per KV head, QL query tokens per sequence.  A consumer warp
 // holds R = G * QL rows: row rho is query token rho / G, head g * G + rho % G.
-// T is the q / out element type, TC the cache's (T, or FP8 E4M3 with scales).
+// T is the q / out element type, TC the cache's (T: an FP8 cache runs on the
+// tensor-core kernel below).
 template <typename T, typename TC, int D, int G, int QL>
-__global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
   constexpr int R = G * QL;
   using S = Shape<TC, D, R>;
   constexpr int NQ = S::EPC / Chunk<T>::N;  // q / out chunks per cache chunk
-  constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
   const int rows_per_seq = QL * p.hq;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -512,12 +469,6 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
   for_each_segment(p, plan, [&](const Segment& seg) -> bool {
     // q of the R rows sharing KV head g, pre-scaled into the exp2 domain
     float qr[R][S::EPL];
-    // FP8 cache: q as f16 pairs, each row scaled by a power of two that puts
-    // its largest element in [2^14, 2^15) (exact for every element above
-    // 2^-29 of that maximum); qmul takes the power back off with the softmax
-    // scale
-    uint32_t qh16[R][S::EPL / 2];
-    float qmul[R];
 #pragma unroll
     for (int h = 0; h < R; ++h) {
       const T* qh =
@@ -529,24 +480,8 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
           const uint4 c = __ldg(reinterpret_cast<const uint4*>(qh) + (lig + S::LPT * k) * NQ + u);
           Chunk<T>::unpack(c, &qr[h][k * S::EPC + u * Chunk<T>::N]);
         }
-      if constexpr (kFp8) {
-        float amax = 0.f;
 #pragma unroll
-        for (int e = 0; e < S::EPL; ++e) amax = fmaxf(amax, fabsf(qr[h][e]));
-#pragma unroll
-        for (int off = 1; off < S::LPT; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const int ex = amax > 0.f ? min(max(14 - ilogbf(amax), -100), 100) : 0;
-        const float up = ldexpf(1.f, ex);
-        qmul[h] = p.scale_log2 * ldexpf(1.f, -ex);
-#pragma unroll
-        for (int e = 0; e < S::EPL; e += 2) {
-          const __half2 v = __floats2half2_rn(qr[h][e] * up, qr[h][e + 1] * up);
-          qh16[h][e / 2] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
-      }
+      for (int e = 0; e < S::EPL; ++e) qr[h][e] *= p.scale_log2;
     }
     float acc[R][S::EPL];
     float m[R], l[R];
@@ -582,28 +517,16 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
           for (int h = 0; h < R; ++h) odd[h] = 0.f;
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
-            if constexpr (kFp8) {
-              uint32_t kh[S::EPC / 2];
-              e4m3x16_to_f16x2(pkv::lds128(row + (lig + S::LPT * k) * 16), kh);
+            float f[S::EPC];
+            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
 #pragma unroll
-              for (int h = 0; h < R; ++h)
+            for (int h = 0; h < R; ++h)
 #pragma unroll
-                for (int e = 0; e < S::EPC / 2; ++e) fma_h2(dot[h], odd[h], qh16[h][k * S::EPC / 2 + e], kh[e]);
-            } else {
-              float f[S::EPC];
-              Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
-#pragma unroll
-              for (int h = 0; h < R; ++h)
-#pragma unroll
-                for (int e = 0; e < S::EPC; e += 2)
-                  fma2(dot[h], odd[h], qr[h][k * S::EPC + e], qr[h][k * S::EPC + e + 1], f[e], f[e + 1]);
-            }
+              for (int e = 0; e < S::EPC; e += 2)
+                fma2(dot[h], odd[h], qr[h][k * S::EPC + e], qr[h][k * S::EPC + e + 1], f[e], f[e + 1]);
           }
 #pragma unroll
-          for (int h = 0; h < R; ++h) {
-            dot[h] += odd[h];
-            if constexpr (kFp8) dot[h] *= qmul[h];
-          }
+          for (int h = 0; h < R; ++h) dot[h] += odd[h];
         }
 #pragma unroll
         for (int h = 0; h < R; ++h) {
@@ -651,26 +574,13 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
           const unsigned char* row = vs + (static_cast<size_t>(tt) * p.hkv + g) * S::ROW_BYTES;
 #pragma unroll
           for (int k = 0; k < S::CPL; ++k) {
-            if constexpr (kFp8) {
-              uint16_t ph[R];
+            float f[S::EPC];
+            Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
 #pragma unroll
-              for (int h = 0; h < R; ++h) ph[h] = __half_as_ushort(__float2half_rn(sc[r][h] * kFp8PScale));
-              uint32_t vh[S::EPC / 2];
-              e4m3x16_to_f16x2(pkv::lds128(row + (lig + S::LPT * k) * 16), vh);
+            for (int h = 0; h < R; ++h)
 #pragma unroll
-              for (int h = 0; h < R; ++h)
-#pragma unroll
-                for (int e = 0; e < S::EPC / 2; ++e)
-                  fma_h1(acc[h][k * S::EPC + 2 * e], acc[h][k * S::EPC + 2 * e + 1], ph[h], vh[e]);
-            } else {
-              float f[S::EPC];
-              Chunk<TC>::unpack(pkv::lds128(row + (lig + S::LPT * k) * 16), f);
-#pragma unroll
-              for (int h = 0; h < R; ++h)
-#pragma unroll
-                for (int e = 0; e < S::EPC; e += 2)
-                  fma2(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], sc[r][h], sc[r][h], f[e], f[e + 1]);
-            }
+              for (int e = 0; e < S::EPC; e += 2)
+                fma2(acc[h][k * S::EPC + e], acc[h][k * S::EPC + e + 1], sc[r][h], sc[r][h], f[e], f[e + 1]);
           }
         }
       }
@@ -678,14 +588,6 @@ __global__ void __launch_bounds__(288, Shape<TC, D, G * QL>::CTAS) paged_decode_
       if (lane == 0) pkv::mbar_arrive(&empty[s]);
     }
 
-    // V's scale (and P's 2^15) is linear in the output: apply it once to the accumulators
-    if constexpr (kFp8) {
-      const float vs_out = p.v_scale / kFp8PScale;
-#pragma unroll
-      for (int h = 0; h < R; ++h)
-#pragma unroll
-        for (int e = 0; e < S::EPL; ++e) acc[h][e] *= vs_out;
-    }
 
     // reduce the token groups of the warp (m is already warp-uniform)
 #pragma unroll
@@ -1484,7 +1386,7 @@ LaunchShape launch_shape(int hkv) {
   ls.stage_bytes = static_cast<size_t>(ls.t_stage) * hkv * S::ROW_BYTES * 2;
   const size_t misc = 2 * kMaxStages * sizeof(uint64_t) + 64 * sizeof(long long) + 32 * sizeof(int) +
                       (ls.wph > 1 ? static_cast<size_t>(ls.nw) * R * (D + 2) * sizeof(float) : 0);
-  int stages = static_cast<int>((kSmemBudget / S::CTAS - misc) / ls.stage_bytes);
+  int stages = static_cast<int>((kSmemBudget - misc) / ls.stage_bytes);
   ls.stages = stages > kMaxStages ? kMaxStages : stages;
   ls.smem = ls.stages * ls.stage_bytes + misc;
   return ls;
@@ -1524,7 +1426,7 @@ int launch(Params& p, int sms, cudaStream_t stream) {
   if (p.num_splits > 0)
     grid = static_cast<unsigned>(static_cast<long long>(p.batch) * p.num_splits);
   else
-    grid = static_cast<unsigned>(sms * kAutoCtasPerSm * Shape<TC, D, G * QL>::CTAS);
+    grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
   if (grid == 0) return PKV_OK;
   kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;

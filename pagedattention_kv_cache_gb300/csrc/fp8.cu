@@ -65,12 +65,11 @@ __global__ void __launch_bounds__(256) kv_store_fp8_kernel(const uint4* __restri
   }
 }
 
-// One query head per KV head: the CUDA-core kernel (two CTAs per SM); two or
-// four: the tensor-core kernel, codes widened to f16 in registers.
+// Every group size runs on the tensor-core kernel, codes widened to f16 in
+// registers, two 16-key chunks per warp per stage.
 template <int G>
 int launch_fp8(Params& p, int sms, cudaStream_t stream) {
-  if constexpr (G >= 2) return launch_mma<G, 1, __nv_fp8_e4m3>(p, sms, stream);
-  else return launch<__nv_bfloat16, __nv_fp8_e4m3, 128, G, 1>(p, sms, stream);
+  return launch_mma<G, 1, __nv_fp8_e4m3>(p, sms, stream);
 }
 
 }  // namespace
