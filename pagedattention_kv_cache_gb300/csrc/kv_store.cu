@@ -19,53 +19,55 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 // A token row (all KV heads of the token) is cpr 16-byte chunks.  Lanes are
 // grouped per token: a group of lpt lanes (cpr rounded up to a power of two,
-// at most 32) takes one token, each lane up to kBatch of its chunks per pass.
-// The slot and every chunk of K and V are loaded before anything is stored,
-// so one round trip to memory covers a whole row.
+// at most 32) takes one piece of kb * lpt chunks of a token, each lane kb
+// (<= kBatch) of them.  The slot and every chunk of the piece are loaded
+// before anything is stored, so one round trip to memory covers it.  Small
+// batches (a decode step's few hundred tokens) take kb = 1 and several pieces
+// per row, so they still spread over the SMs.
 constexpr int kBatch = 4;
 constexpr int kBlocksPerSm = 4;  // resident blocks of 256 threads at this kernel's register count
 
 __global__ void __launch_bounds__(256, kBlocksPerSm) kv_store_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                                       const int32_t* __restrict__ slot_mapping, int32_t num_tokens,
-                                                       int32_t cpr, int32_t lpt, int64_t num_slots,
-                                                       unsigned int* err) {
+                                                       const int32_t* __restrict__ slot_mapping, int64_t units,
+                                                       int32_t pieces, int32_t cpr, int32_t lpt, int32_t kb,
+                                                       int64_t num_slots, unsigned int* err) {
   const int lane = threadIdx.x % 32;
-  const int sub = lane / lpt;       // token of this lane inside the warp's group
-  const int cl = lane % lpt;        // first chunk of this lane
-  const int tpw = 32 / lpt;         // tokens per warp pass
+  const int sub = lane / lpt;  // unit of this lane inside the warp's group
+  const int cl = lane % lpt;
+  const int upw = 32 / lpt;    // units per warp pass
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
-  for (int64_t t0 = warp * tpw; t0 < num_tokens; t0 += nwarps * tpw) {
-    const int64_t token = t0 + sub;
-    if (token >= num_tokens) continue;
+  for (int64_t u0 = warp * upw; u0 < units; u0 += nwarps * upw) {
+    const int64_t unit = u0 + sub;
+    if (unit >= units) continue;
+    const int64_t token = unit / pieces;
+    const int c0 = static_cast<int>(unit - token * pieces) * kb * lpt + cl;  // this lane's first chunk
     const int32_t slot = __ldg(slot_mapping + token);
     const uint4* ks = k + token * cpr;
     const uint4* vs = v + token * cpr;
-    for (int c0 = cl; c0 < cpr; c0 += kBatch * lpt) {
-      uint4 kr[kBatch], vr[kBatch];
+    uint4 kr[kBatch], vr[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int c = c0 + u * lpt;
-        if (c < cpr) {
-          kr[u] = ld_stream(ks + c);
-          vr[u] = ld_stream(vs + c);
-        }
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = c0 + u * lpt;
+      if (u < kb && c < cpr) {
+        kr[u] = ld_stream(ks + c);
+        vr[u] = ld_stream(vs + c);
       }
-      if (slot == -1) continue;
-      if (slot < 0 || slot >= num_slots) {
-        if (c0 == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);
-        continue;
-      }
-      uint4* kd = k_cache + static_cast<int64_t>(slot) * cpr;
-      uint4* vd = v_cache + static_cast<int64_t>(slot) * cpr;
+    }
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) {
+      if (c0 == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);
+      continue;
+    }
+    uint4* kd = k_cache + static_cast<int64_t>(slot) * cpr;
+    uint4* vd = v_cache + static_cast<int64_t>(slot) * cpr;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int c = c0 + u * lpt;
-        if (c < cpr) {
-          kd[c] = kr[u];
-          vd[c] = vr[u];
-        }
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = c0 + u * lpt;
+      if (u < kb && c < cpr) {
+        kd[c] = kr[u];
+        vd[c] = vr[u];
       }
     }
   }
@@ -98,13 +100,18 @@ extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v
   int32_t lpt = 1;
   while (lpt < cpr && lpt < 32) lpt *= 2;
   const int threads = 256;
-  const int64_t tokens_per_block = (threads / 32) * (32 / lpt);
-  int64_t blocks = (num_tokens + tokens_per_block - 1) / tokens_per_block;
   const int64_t cap = static_cast<int64_t>(info.sms) * kBlocksPerSm;
+  // kBatch chunks per lane once the batch fills every resident warp, else one
+  const int64_t units_full = static_cast<int64_t>(num_tokens) * ((cpr + kBatch * lpt - 1) / (kBatch * lpt));
+  const int32_t kb = units_full * lpt / 32 >= cap * (threads / 32) ? kBatch : 1;
+  const int32_t pieces = (cpr + kb * lpt - 1) / (kb * lpt);
+  const int64_t units = static_cast<int64_t>(num_tokens) * pieces;
+  const int64_t units_per_block = (threads / 32) * (32 / lpt);
+  int64_t blocks = (units + units_per_block - 1) / units_per_block;
   if (blocks > cap) blocks = cap;
   kv_store_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, cpr, lpt,
+      static_cast<uint4*>(v_cache), slot_mapping, units, pieces, cpr, lpt, kb,
       static_cast<int64_t>(num_blocks) * block_size, err);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
