@@ -116,7 +116,8 @@ int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
  * Bytes of split workspace pkv_paged_decode_attn needs on the current device
  * for these sizes (0 when num_splits == 1).  num_splits: 0 = automatic
  * (the context tokens of the whole batch are divided evenly over a grid sized
- * to the GPU), S >= 1 = every sequence's context cut into S equal parts.
+ * to the GPU), S >= 1 = every sequence's context cut into S equal parts (on
+ * the tensor-core path, split points are rounded up to multiples of 16 tokens).
  * Returns 0 and sets nothing on invalid sizes; a CUDA query failure also returns 0.
  */
 size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,

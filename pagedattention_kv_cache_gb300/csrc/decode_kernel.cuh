@@ -93,7 +93,7 @@ struct Params {
   const int32_t* context_lens;
   float* part_o;     // [slots, QL * Hq, D]
   float* part_ml;    // [slots, QL * Hq, 2]
-  int32_t* counters; // [batch]
+  int32_t* counters; // [batch] sequence tickets, then [slots] merge-group tickets
   unsigned int* err;
   int max_blocks;
   int batch;
@@ -264,109 +264,155 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
   return true;
 }
 
-// Called by all consumer threads after this CTA wrote its part of a split
-// sequence: the part that arrives last (atomic ticket, nothing waits) merges
-// every part's (o, m, l) by log-sum-exp and writes the output.  A warp takes
-// four output rows at a time so their loads overlap: one pass over the parts
+// Log-sum-exp merge of `count` partial states (o, m, l) of one sequence, at
+// workspace slots first + i * step.  With `final` the normalized rows go to the
+// output; otherwise the merged state is written over slot `first` (each row is
+// read and written by one warp only, so the in-place write is safe).  A warp
+// takes four rows at a time so their loads overlap: one pass over the parts
 // folds each lane's share of (m, l) online and the lanes combine them by
 // shuffles; a second pass sums the weighted rows, each lane owning D / 32
-// columns, eight parts per step.  A long context split over dozens of CTAs
-// then merges in a few round trips to L2 instead of a few per row.
+// columns, eight parts per step.
 template <typename T, int D>
-__device__ __forceinline__ void combine_if_last(const Params& p, const Segment& seg, int rows_per_seq, int* sh_flag,
-                                                int nthreads_c) {
+__device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg, int rows_per_seq, int first,
+                                            int step, int count, bool final, int nthreads_c) {
   constexpr int RW = 4;  // rows a warp merges together
+  constexpr int PER = D / 32;
   const int tid = threadIdx.x;
-  pkv::named_barrier_sync(1, nthreads_c);
-  if (tid == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(p.counters + seg.b, 1);
-    sh_flag[0] = ticket == seg.nparts - 1;
-  }
-  pkv::named_barrier_sync(1, nthreads_c);
-  if (sh_flag[0]) {
-    __threadfence();
-    constexpr int PER = D / 32;
-    const int warp = tid / 32;
-    const int lane = tid % 32;
-    const int nwarps = nthreads_c / 32;
-    const int np = seg.nparts;
-    T* out = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
-    const size_t ml_stride = static_cast<size_t>(rows_per_seq) * 2;
-    const size_t o_stride = static_cast<size_t>(rows_per_seq) * D;
-    const float* ml_base = p.part_ml + static_cast<size_t>(seg.first_slot) * rows_per_seq * 2;
-    const float* o_base = p.part_o + static_cast<size_t>(seg.first_slot) * rows_per_seq * D + lane * PER;
-    for (int row0 = warp * RW; row0 < rows_per_seq; row0 += nwarps * RW) {
-      float mm[RW], ll[RW];
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+  const int nwarps = nthreads_c / 32;
+  T* out = static_cast<T*>(p.out) + static_cast<size_t>(seg.b) * rows_per_seq * D;
+  const size_t ml_stride = static_cast<size_t>(step) * rows_per_seq * 2;
+  const size_t o_stride = static_cast<size_t>(step) * rows_per_seq * D;
+  float* ml_base = p.part_ml + static_cast<size_t>(first) * rows_per_seq * 2;
+  float* o_base = p.part_o + static_cast<size_t>(first) * rows_per_seq * D + lane * PER;
+  for (int row0 = warp * RW; row0 < rows_per_seq; row0 += nwarps * RW) {
+    float mm[RW], ll[RW];
 #pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        mm[r] = -INFINITY;
-        ll[r] = 0.f;
-      }
-      // (m, l) of this lane's parts, folded online
-      for (int j = lane; j < np; j += 32) {
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          if (row0 + r >= rows_per_seq) continue;
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_base + j * ml_stride + (row0 + r) * 2));
-          const float mn = fmaxf(mm[r], v.x);
-          if (mn != -INFINITY) {
-            ll[r] = ll[r] * exp2f(mm[r] - mn) + v.y * exp2f(v.x - mn);
-            mm[r] = mn;
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < RW; ++r) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float mo = __shfl_xor_sync(0xffffffffu, mm[r], off);
-          const float lo = __shfl_xor_sync(0xffffffffu, ll[r], off);
-          const float mn = fmaxf(mm[r], mo);
-          if (mn != -INFINITY) {
-            ll[r] = ll[r] * exp2f(mm[r] - mn) + lo * exp2f(mo - mn);
-            mm[r] = mn;
-          }
-        }
-      }
-      float acc[RW][PER];
-#pragma unroll
-      for (int r = 0; r < RW; ++r)
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[r][e] = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < np; ++j) {
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          if (row0 + r >= rows_per_seq) continue;
-          const float w = exp2f(__ldcg(ml_base + j * ml_stride + (row0 + r) * 2) - mm[r]);
-          const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
-          float v[PER];
-          if constexpr (PER == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-            v[0] = x.x;
-            v[1] = x.y;
-            v[2] = x.z;
-            v[3] = x.w;
-          } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-            v[0] = x.x;
-            v[1] = x.y;
-          }
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[e], acc[r][e]);
-        }
-      }
+    for (int r = 0; r < RW; ++r) {
+      mm[r] = -INFINITY;
+      ll[r] = 0.f;
+    }
+    // (m, l) of this lane's parts, folded online
+    for (int j = lane; j < count; j += 32) {
 #pragma unroll
       for (int r = 0; r < RW; ++r) {
         if (row0 + r >= rows_per_seq) continue;
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_base + j * ml_stride + (row0 + r) * 2));
+        const float mn = fmaxf(mm[r], v.x);
+        if (mn != -INFINITY) {
+          ll[r] = ll[r] * exp2f(mm[r] - mn) + v.y * exp2f(v.x - mn);
+          mm[r] = mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mm[r], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, ll[r], off);
+        const float mn = fmaxf(mm[r], mo);
+        if (mn != -INFINITY) {
+          ll[r] = ll[r] * exp2f(mm[r] - mn) + lo * exp2f(mo - mn);
+          mm[r] = mn;
+        }
+      }
+    }
+    float acc[RW][PER];
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[r][e] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < count; ++j) {
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        if (row0 + r >= rows_per_seq) continue;
+        const float w = exp2f(__ldcg(ml_base + j * ml_stride + (row0 + r) * 2) - mm[r]);
+        const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
+        float v[PER];
+        if constexpr (PER == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+          v[0] = x.x;
+          v[1] = x.y;
+          v[2] = x.z;
+          v[3] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+          v[0] = x.x;
+          v[1] = x.y;
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[e], acc[r][e]);
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      if (row0 + r >= rows_per_seq) continue;
+      if (final) {
         const float inv = 1.f / ll[r];
 #pragma unroll
         for (int e = 0; e < PER; ++e)
           out[static_cast<size_t>(row0 + r) * D + lane * PER + e] = static_cast<T>(acc[r][e] * inv);
+      } else {
+        float* dst = o_base + static_cast<size_t>(row0 + r) * D;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) dst[e] = acc[r][e];
+        if (lane == 0) *reinterpret_cast<float2*>(ml_base + (row0 + r) * 2) = make_float2(mm[r], ll[r]);
       }
     }
-    if (tid == 0) p.counters[seg.b] = 0;
+  }
+}
+
+// Parts of a split sequence merged per group of this many consecutive parts.
+constexpr int kMergeGroup = 8;
+
+// Called by all consumer threads after this CTA wrote its part of a split
+// sequence.  Nothing waits on another CTA: atomic tickets elect the mergers.
+// The part that arrives last in its group of kMergeGroup consecutive parts
+// merges the group into the group's first slot; the group merger that
+// arrives last merges the groups and writes the output (a sequence of at most
+// kMergeGroup parts is merged straight to the output).  A long context split
+// over ~150 parts thus merges in two short steps spread over ~20 CTAs instead
+// of one CTA reading every part.
+template <typename T, int D>
+__device__ __forceinline__ void combine_if_last(const Params& p, const Segment& seg, int rows_per_seq, int* sh_flag,
+                                                int nthreads_c) {
+  const int tid = threadIdx.x;
+  const int np = seg.nparts;
+  const int part = seg.slot - seg.first_slot;
+  const int gfirst = part / kMergeGroup * kMergeGroup;
+  const int gsize = min(kMergeGroup, np - gfirst);
+  const int ng = (np + kMergeGroup - 1) / kMergeGroup;
+  int* gcount = p.counters + p.batch + seg.first_slot + gfirst;
+  pkv::named_barrier_sync(1, nthreads_c);
+  if (tid == 0) {
+    __threadfence();
+    sh_flag[0] = atomicAdd(gcount, 1) == gsize - 1;
+  }
+  pkv::named_barrier_sync(1, nthreads_c);
+  if (sh_flag[0]) {
+    __threadfence();
+    if (ng == 1) {
+      merge_parts<T, D>(p, seg, rows_per_seq, seg.first_slot, 1, np, true, nthreads_c);
+      if (tid == 0) *gcount = 0;
+    } else {
+      merge_parts<T, D>(p, seg, rows_per_seq, seg.first_slot + gfirst, 1, gsize, false, nthreads_c);
+      pkv::named_barrier_sync(1, nthreads_c);
+      if (tid == 0) {
+        *gcount = 0;
+        __threadfence();
+        sh_flag[0] = atomicAdd(p.counters + seg.b, 1) == ng - 1;
+      }
+      pkv::named_barrier_sync(1, nthreads_c);
+      if (sh_flag[0]) {
+        __threadfence();
+        merge_parts<T, D>(p, seg, rows_per_seq, seg.first_slot, kMergeGroup, ng, true, nthreads_c);
+        if (tid == 0) p.counters[seg.b] = 0;
+      }
+    }
   }
   pkv::named_barrier_sync(1, nthreads_c);
 }
@@ -1403,7 +1449,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 size_t workspace_layout(int batch, int hq, int d, int num_splits, int sms, size_t* off_o, size_t* off_ml) {
   const size_t slots = slot_count(batch, num_splits, sms);
   if (slots == 0) return 0;
-  const size_t counters = align256(static_cast<size_t>(batch) * sizeof(int32_t));
+  // tickets: one per sequence, then one per slot (the merge groups)
+  const size_t counters = align256((static_cast<size_t>(batch) + slots) * sizeof(int32_t));
   *off_o = counters;
   *off_ml = counters + align256(slots * hq * d * sizeof(float));
   return *off_ml + align256(slots * hq * 2 * sizeof(float));

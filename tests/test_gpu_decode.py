@@ -89,6 +89,27 @@ def test_mma_kernel_stage_layouts(kv_heads, block_size, splits):
     run_decode(w, num_splits=splits, poison=True)
 
 
+# Many parts per sequence: the parts merge in groups of 8 (the last arrival of a
+# group merges it), then the last group merger merges the groups.  Covers one
+# group, a partial last group, and ~150 automatic parts; G = 2 runs the CUDA-core
+# kernel, G = 4 the tensor-core kernel.
+@pytest.mark.parametrize("group,dtype", [(2, torch.float32), (4, torch.bfloat16)])
+@pytest.mark.parametrize("lens,splits", [([60000], 0), ([20000, 3, 40000], 0), ([9000, 700], 9), ([5000], 8),
+                                         ([30000, 1], 23)])
+def test_grouped_merge_of_many_parts(group, dtype, lens, splits):
+    rng = np.random.default_rng(sum(lens) + splits + group)
+    bs = 16
+    nb = sum(math.ceil(n / bs) for n in lens) + 5
+    perm = rng.permutation(nb).tolist()
+    tables, pos = [], 0
+    for n in lens:
+        k = math.ceil(n / bs)
+        tables.append(perm[pos:pos + k])
+        pos += k
+    w = wl.DecodeWorkload("many-parts", 91, 2 * group, 2, 128, bs, nb, dtype, lens, tables)
+    run_decode(w, num_splits=splits)
+
+
 def test_long_context_split_decode_full_size():
     r = run_decode(wl.long_context_decode(), gen_device="cuda", check_store=True)
     assert r["stats"]["mean_abs"] < 1e-3
