@@ -546,6 +546,91 @@ def bench_kv_store(args, device):
     return result
 
 
+def bench_cuda_graph(args, device):
+    """Small-batch decode (batch 8, the same Qwen3-0.6B shape, 28 layers of store + decode):
+    eager launches against one replay of the step captured in a CUDA graph."""
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b256_28l(batch=8)
+    st = DecodeState(w, device)
+    L = w.num_layers
+    reps = max(20, args.steps)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    eager_ms = timed(st.step)
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        st.step()
+    torch.cuda.current_stream(device).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        st.step()
+    graph_ms = timed(graph.replay)
+    assert st.pkv.device_error() == 0
+    step_bytes = L * (decode_alg_bytes(w) + store_alg_bytes(w.batch, w))
+    gbs = step_bytes / (graph_ms * 1e-3) / 1e9
+    hbm_peak = measured_peaks()[0]
+    del st, graph
+    torch.cuda.empty_cache()
+    return {"workload": w.name.replace("b256", "b8"), "batch": w.batch, "layers": L,
+            "launches_per_step": 2 * L, "eager_ms_per_step": round(eager_ms, 4),
+            "graph_ms_per_step": round(graph_ms, 4), "speedup": round(eager_ms / graph_ms, 3),
+            "value": round(gbs, 1), "unit": UNIT, "decode_tokens_per_s": round(w.batch / (graph_ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / hbm_peak, 4)},
+            "l2": "inputs (~4 GB per step) larger than L2, no flush"}
+
+
+def bench_copy_blocks(args, device):
+    """Copy-on-write burst: 64 block pairs across 28 layers' K and V pools (block size 256,
+    8 KV heads, head_dim 128, bf16: 512 KiB per block per pool), L2 flushed before each rep."""
+    import pagedattention_kv_cache_gb300 as pkv
+
+    L, pairs, bs, hkv, d = 28, 64, 256, 8, 128
+    nb = 2 * pairs
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1008)
+    ks = [torch.randn(nb, bs, hkv, d, generator=gen, device=device).bfloat16() for _ in range(L)]
+    vs = [torch.randn(nb, bs, hkv, d, generator=gen, device=device).bfloat16() for _ in range(L)]
+    dst = pairs + torch.randperm(pairs, generator=gen, device=device)
+    bp = torch.stack([torch.arange(pairs, device=device), dst], dim=1).to(torch.int32).contiguous()
+    flush = L2Flush(device)
+    times = []
+    for i in range(args.warmup + max(10, args.steps)):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.copy_blocks(ks, vs, bp)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    assert pkv.device_error() == 0
+    ms = statistics.median(times)
+    nbytes = pairs * L * 2 * (bs * hkv * d * 2) * 2 + pairs * 8
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = measured_peaks()[0]
+    del ks, vs
+    torch.cuda.empty_cache()
+    return {"workload": f"copy-blocks-{pairs}pairs-{L}layers-bs{bs}", "pairs": pairs, "layers": L,
+            "alg_bytes": nbytes, "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
+            "kernel": "copy_blocks_kernel",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+
+
 class L2Flush:
     """Between timed reps: write a buffer twice the size of L2, then read another one as large,
     so L2 holds none of the timed call's inputs and no dirty lines whose write-back would land
@@ -723,6 +808,8 @@ def run_ours(args):
     line["verify"] = bench_verify(args, device)
     line["long_context"] = bench_long_context(args, device)
     line["kv_store"] = bench_kv_store(args, device)
+    line["cuda_graph_decode"] = bench_cuda_graph(args, device)
+    line["copy_blocks"] = bench_copy_blocks(args, device)
     from pagedattention_kv_cache_gb300 import workloads as wl
     lh = bench_prefill(args, device, wl.long_history_prefill())
     lh["roofline"] = {"bound": "tensor", "achieved": lh["tflops"], "peak": prefill["roofline"]["peak"],
