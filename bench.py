@@ -793,7 +793,7 @@ def run_ours(args):
         "decode_tokens_per_s": round(world * w.batch / (res["ms_step"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": decode_traffic_record(),
-                     "kernel": "paged_decode_kernel", "alg_bytes_per_launch": dec_bytes,
+                     "kernel": "paged_decode_mma_kernel<G=2>", "alg_bytes_per_launch": dec_bytes,
                      "ms_per_launch": round(dec_ms, 5), "peak_source": f"{peak_src} HBM copy"},
         "e2e": e2e,
         "prefill": prefill,

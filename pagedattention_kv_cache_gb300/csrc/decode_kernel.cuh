@@ -1531,8 +1531,12 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
 template <typename T, int D>
 int dispatch_g(Params& p, int group, int sms, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch<T, T, D, 1, 1>(p, sms, stream);
-    case 2: return launch<T, T, D, 2, 1>(p, sms, stream);
+    case 1:
+      if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) return launch_mma<1, 1>(p, sms, stream);
+      return launch<T, T, D, 1, 1>(p, sms, stream);
+    case 2:
+      if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) return launch_mma<2, 1>(p, sms, stream);
+      return launch<T, T, D, 2, 1>(p, sms, stream);
     case 4:
       if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) return launch_mma<4, 1>(p, sms, stream);
       return launch<T, T, D, 4, 1>(p, sms, stream);

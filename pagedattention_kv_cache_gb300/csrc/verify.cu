@@ -11,12 +11,11 @@
 
 namespace {
 
-// Rows per KV head R = G * q_len: the CUDA-core kernel for R <= 2, the
-// tensor-core (mma.sync) kernel for 3 <= R <= 16.
+// Rows per KV head R = G * q_len <= 16: the tensor-core (mma.sync) kernel,
+// the same one bf16 decode with head_dim 128 runs on (so q_len 1 is decode).
 template <int G, int QL>
 int launch_rows(Params& p, int sms, cudaStream_t stream) {
-  if constexpr (G * QL <= 2) return launch<__nv_bfloat16, __nv_bfloat16, 128, G, QL>(p, sms, stream);
-  else return launch_mma<G, QL>(p, sms, stream);
+  return launch_mma<G, QL>(p, sms, stream);
 }
 
 template <int G>
