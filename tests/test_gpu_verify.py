@@ -65,6 +65,40 @@ def test_verify_block_sizes(block_size):
         run_verify(w, 4, splits)
 
 
+def test_verify_batch256_q4_full_size_sampled():
+    # the bench's verify case at full size (batch 256, one layer, q_len 4) in the launch it times;
+    # the longest, the shortest and six random sequences are checked against the oracle one by one
+    q_len = 4
+    w = wl.qwen3_decode_b256_28l(num_layers=1)
+    t = wl.verify_tensors(w, q_len, "cuda")
+    pm = md.prefill_metadata(w.block_tables, [n - q_len for n in w.context_lens], [q_len] * w.batch, w.block_size)
+    dm = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), "cuda")
+    pkv.kv_store(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], torch.from_numpy(pm["slot_mapping"]).cuda())
+    out = pkv.paged_verify_attn(t["q"], t["k_cache"], t["v_cache"], dm["block_tables"], dm["context_lens"], w.scale)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    lens = np.asarray(w.context_lens)
+    rng = np.random.default_rng(8)
+    pick = sorted({int(lens.argmax()), int(lens.argmin())} | set(rng.choice(w.batch, 6, replace=False).tolist()))
+    for b in pick:
+        table = torch.tensor(w.block_tables[b], device="cuda", dtype=torch.long)
+        kb, vb = as_np(t["k_cache"][table]), as_np(t["v_cache"][table])
+        n = int(lens[b])
+        local = list(range(len(w.block_tables[b])))
+        om_ = om.prepare_prefill([dict(block_table=local, num_cached_tokens=n - q_len, num_scheduled_tokens=q_len)],
+                                 w.block_size)
+        # the stored rows of this sequence, bit for bit
+        rows = np.arange(n - q_len, n)
+        for i, pos in enumerate(rows):
+            blk, off = divmod(int(pos), w.block_size)
+            assert np.array_equal(bits(t["k_cache"][table[blk], off]), bits(t["k_new"][b * q_len + i]))
+        _, _, hq, d = t["q"].shape
+        ref = oa.paged_prefill_attention(as_np(t["q"][b]).reshape(q_len, hq, d), om_["cu_seqlens_q"],
+                                         om_["cu_seqlens_k"], w.scale, k_cache=kb, v_cache=vb,
+                                         block_tables=om.padded_block_tables([local]))
+        assert_close(out[b], ref, w.dtype, f"verify batch-256 sequence {b}")
+
+
 def test_verify_qwen3_batch32_q4():
     w = wl.qwen3_decode_b32()
     run_verify(w, 4)
