@@ -10,23 +10,22 @@
 // with K_t / V_t at physical block block_tables[b, t / bs], offset t % bs.
 // context_lens 0 writes zeros and reads nothing.
 //
-// How (GB300 design):
+// How (GB300 design), shared by both kernels below:
 //  * A CTA covers every KV head of a token range, so each token's K (or V)
 //    row of all heads, [Hkv, D], is contiguous in the [blocks, bs, Hkv, D]
-//    pool and a run of tokens inside one block is one contiguous span.  One
-//    producer lane streams those spans into a ring of shared-memory stages with
-//    1-D bulk (TMA) copies completed on mbarriers; every K/V byte is read from
-//    HBM exactly once, and all G query heads of a KV head reuse it on chip.
-//  * One consumer warp per (KV head, token phase).  Within a warp LPT lanes
-//    share a token (16-byte conflict-free shared loads, fp32 dot products,
-//    xor-shuffle reduction); scores of a stage are reduced to a stage maximum
-//    and folded into a running online softmax (exp2 domain), then P.V is
-//    accumulated in registers.
+//    pool.  A producer warp streams the range into a ring of shared-memory
+//    stages with TMA copies completed on mbarriers; every K/V byte is read from
+//    HBM once, and all G query heads of a KV head reuse it on chip.
+//  * Consumer warps, one per (KV head, token phase), fold each stage into a
+//    running online softmax (exp2 domain) and accumulate P.V.
 //  * Split over the context: the batch's context tokens, flattened, are
 //    divided evenly over the grid (automatic mode) or each sequence into S
 //    equal parts.  A sequence covered by one CTA is written directly; otherwise
-//    each part writes (o, m, l) to the workspace and the last CTA to finish
-//    a sequence (atomic ticket, no waiting) merges the parts by log-sum-exp.
+//    each part writes (o, m, l) to the workspace and atomic tickets (no
+//    waiting) elect the CTAs that merge the parts by log-sum-exp.
+// paged_decode_mma_kernel (mma.sync tensor cores, 16-token tensor copies)
+// runs every bf16 or FP8 cache with head_dim 128; paged_decode_kernel (CUDA
+// cores, 1-D bulk copies of token spans) runs fp32 caches and head_dim 64.
 //
 // Verify (speculative-decoding target pass, QL > 1): query token i of
 // sequence b sits at position context_lens[b] - QL + i and attends keys up to
@@ -1138,8 +1137,6 @@ __global__ void __launch_bounds__(288, 1)
         for (int sub = 0; sub < NSUB; ++sub) {
           if (nt <= tw0 + sub * kMmaTokens) continue;
           const uint32_t vbase = stage_addr + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub;
-          const unsigned char* vstage = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub;
-          (void)vstage;
           uint32_t pf[4];
           if constexpr (kFp8) {
             // P as f16 times 2^7; l sums the same rounded weights
@@ -1161,6 +1158,7 @@ __global__ void __launch_bounds__(288, 1)
             // O^T += V^T P^T: the A fragment pairs keys (2c, 2c+1) and (2c+8, 2c+9)
             // of one head_dim index by byte permutes of 16 codes of each key row;
             // m-tile t, row m stands for head_dim 16 m + 2t (m < 8) or 16 (m - 8) + 2t + 1
+            const unsigned char* vstage = stage_base + s * p.stage_bytes + p.stage_bytes / 2 + sub * csub;
             const uint4 ra = pkv::lds128(vstage + v8a);
             const uint4 rb = pkv::lds128(vstage + v8b);
             const uint4 rc = pkv::lds128(vstage + v8a + 8 * rs);
