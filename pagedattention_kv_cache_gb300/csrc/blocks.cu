@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant_
                                                           const int32_t* __restrict__ pairs, int32_t num_pairs,
                                                           int32_t num_layers, int32_t num_blocks,
                                                           int64_t chunks_per_block, unsigned int* err) {
+  pkv::pdl_enter();
   const int64_t per_pair = chunks_per_block * 2 * num_layers;
   const int64_t total = per_pair * num_pairs;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -68,7 +69,7 @@ extern "C" int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(info.sms) * 8;
   if (blocks > cap) blocks = cap;
-  copy_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(pools, block_pairs, num_pairs, num_layers,
-                                                                      num_blocks, chunks_per_block, err);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  const cudaError_t e = pkv::launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                                        pools, block_pairs, num_pairs, num_layers, num_blocks, chunks_per_block, err);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pagedkv.h"
 
 namespace pkv {
@@ -38,6 +40,24 @@ int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64
 // (E4M3 codes, box of 128, one copy).
 int encode_paged_kv(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks,
                     int elem_bytes);
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization allowed (see pdl_enter).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -120,6 +140,17 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with launch_pdl, so it may be scheduled while the previous kernel in the
+// stream is still running; its first statement is pdl_enter(): it lets the
+// next kernel be scheduled in turn, then waits until every earlier kernel has
+// completed and its writes are visible.  Only the launch latency and CTA
+// scheduling overlap: no global memory is touched before the wait.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {

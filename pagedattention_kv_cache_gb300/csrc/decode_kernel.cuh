@@ -422,6 +422,7 @@ __device__ __forceinline__ void combine_if_last(const Params& p, const Segment& 
 // tensor-core kernel below).
 template <typename T, typename TC, int D, int G, int QL>
 __global__ void __launch_bounds__(288, 1) paged_decode_kernel(const Params p) {
+  pkv::pdl_enter();
   constexpr int R = G * QL;
   using S = Shape<TC, D, R>;
   constexpr int NQ = S::EPC / Chunk<T>::N;  // q / out chunks per cache chunk
@@ -788,6 +789,7 @@ template <int G, int QL, typename TC = __nv_bfloat16>
 __global__ void __launch_bounds__(288, 1)
     paged_decode_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
+  pkv::pdl_enter();
   using T = __nv_bfloat16;
   constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
   constexpr int ES = static_cast<int>(sizeof(TC));  // bytes per cache element
@@ -1473,8 +1475,8 @@ int launch(Params& p, int sms, cudaStream_t stream) {
   else
     grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
   if (grid == 0) return PKV_OK;
-  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  return pkv::launch_pdl(kernel, dim3(grid), dim3((ls.nw + 1) * 32), ls.smem, stream, p) == cudaSuccess ? PKV_OK
+                                                                                                       : PKV_ECUDA;
 }
 
 template <int G, int QL, typename TC = __nv_bfloat16>
@@ -1522,8 +1524,10 @@ int launch_mma(Params& p, int sms, cudaStream_t stream) {
   else
     grid = static_cast<unsigned>(sms * kAutoCtasPerSm);
   if (grid == 0) return PKV_OK;
-  kernel<<<grid, (ls.nw + 1) * 32, ls.smem, stream>>>(p, maps[0], maps[1]);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  return pkv::launch_pdl(kernel, dim3(grid), dim3((ls.nw + 1) * 32), ls.smem, stream, p, maps[0], maps[1]) ==
+                 cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
 }
 
 template <typename T, int D>

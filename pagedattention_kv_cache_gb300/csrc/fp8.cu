@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) kv_store_fp8_kernel(const uint4* __restri
                                                            int64_t total_chunks, int32_t chunks_per_row,
                                                            int64_t num_slots, float k_scale, float v_scale,
                                                            unsigned int* err) {
+  pkv::pdl_enter();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total_chunks;
        idx += stride) {
@@ -97,11 +98,11 @@ extern "C" int pkv_kv_store_fp8(const void* k, const void* v, void* k_cache, voi
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(info.sms) * 8;
   if (blocks > cap) blocks = cap;
-  kv_store_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, total, chunks_per_row, static_cast<int64_t>(num_blocks) * block_size,
-      k_scale, v_scale, err);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  const cudaError_t e = pkv::launch_pdl(
+      kv_store_fp8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, static_cast<const uint4*>(k),
+      static_cast<const uint4*>(v), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, total,
+      chunks_per_row, static_cast<int64_t>(num_blocks) * block_size, k_scale, v_scale, err);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 extern "C" int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,

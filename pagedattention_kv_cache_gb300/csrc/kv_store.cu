@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256, kBlocksPerSm) kv_store_kernel(const uint4
                                                        const int32_t* __restrict__ slot_mapping, int64_t units,
                                                        int32_t pieces, int32_t cpr, int32_t lpt, int32_t kb,
                                                        int64_t num_slots, unsigned int* err) {
+  pkv::pdl_enter();
   const int lane = threadIdx.x % 32;
   const int sub = lane / lpt;  // unit of this lane inside the warp's group
   const int cl = lane % lpt;
@@ -109,9 +110,9 @@ extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v
   const int64_t units_per_block = (threads / 32) * (32 / lpt);
   int64_t blocks = (units + units_per_block - 1) / units_per_block;
   if (blocks > cap) blocks = cap;
-  kv_store_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, units, pieces, cpr, lpt, kb,
-      static_cast<int64_t>(num_blocks) * block_size, err);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  const cudaError_t e = pkv::launch_pdl(
+      kv_store_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, static_cast<const uint4*>(k),
+      static_cast<const uint4*>(v), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, units,
+      pieces, cpr, lpt, kb, static_cast<int64_t>(num_blocks) * block_size, err);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

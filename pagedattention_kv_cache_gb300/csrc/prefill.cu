@@ -126,6 +126,7 @@ __device__ __forceinline__ void load_kv_tile(const Params& p, int seq, int g, in
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
+  pkv::pdl_enter();
   constexpr int TQ = kBM / G;  // query tokens per tile
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t sq = pkv::smem_u32(smem);
@@ -326,8 +327,7 @@ int launch(const Params& p, int max_seqlen_q, cudaStream_t stream) {
     return PKV_ECUDA;
   dim3 grid((max_seqlen_q + TQ - 1) / TQ, p.batch, p.hkv);
   if (grid.x == 0) return PKV_OK;
-  kernel<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  return pkv::launch_pdl(kernel, grid, dim3(kThreads), smem, stream, p) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 }  // namespace

@@ -201,6 +201,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  pdl_enter();
   constexpr int TQ = kBM / G;
   // blocks launch in linear order: x runs over (sequence, KV head), y over
   // query tiles from the last (most keys under the causal mask) to the first,
@@ -666,8 +667,8 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
       cudaSuccess)
     return PKV_ECUDA;
   dim3 grid(a.batch * a.hkv, p.q_tiles * p.parts_max);
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, tm_q, tm_k, tm_v, p) == cudaSuccess ? PKV_OK
+                                                                                                  : PKV_ECUDA;
 }
 
 }  // namespace
