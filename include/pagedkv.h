@@ -39,6 +39,13 @@
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *    nothing synchronises.  Argument errors are detected on the host and
  *    returned as a negative pkv_status before anything is launched.
+ *  - Kernels are launched with programmatic dependent launch: each one waits
+ *    for every earlier kernel in the stream to complete before touching
+ *    memory, and releases the next kernel for scheduling at its start.  A
+ *    caller's own kernel launched with programmatic stream serialization
+ *    after one of these must therefore execute griddepcontrol.wait (or
+ *    cudaGridDependencySynchronize) before reading this library's outputs,
+ *    as that launch mode requires anyway.
  *  - Indices read on the device (slots, block ids, context lengths, cu_seqlens)
  *    are range-checked by the kernels: an out-of-range value skips the access
  *    and raises a bit in the per-device error word (pkv_get_device_error);
