@@ -323,28 +323,45 @@ __device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg,
     for (int r = 0; r < RW; ++r)
 #pragma unroll
       for (int e = 0; e < PER; ++e) acc[r][e] = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < count; ++j) {
+    // kJ parts at a time: every load of a batch is issued before the first is
+    // used, so a batch costs one round trip to L2
+    constexpr int kJ = 4;
+    for (int j0 = 0; j0 < count; j0 += kJ) {
+      float v[kJ][RW][PER];
+      float mj[kJ][RW];
 #pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        if (row0 + r >= rows_per_seq) continue;
-        const float w = exp2f(__ldcg(ml_base + j * ml_stride + (row0 + r) * 2) - mm[r]);
-        const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
-        float v[PER];
-        if constexpr (PER == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-          v[0] = x.x;
-          v[1] = x.y;
-          v[2] = x.z;
-          v[3] = x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-          v[0] = x.x;
-          v[1] = x.y;
+      for (int jj = 0; jj < kJ; ++jj)
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+          mj[jj][r] = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) v[jj][r][e] = 0.f;
+          if (j0 + jj >= count || row0 + r >= rows_per_seq) continue;
+          const size_t j = j0 + jj;
+          mj[jj][r] = __ldcg(ml_base + j * ml_stride + (row0 + r) * 2);
+          const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
+          if constexpr (PER == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+            v[jj][r][0] = x.x;
+            v[jj][r][1] = x.y;
+            v[jj][r][2] = x.z;
+            v[jj][r][3] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            v[jj][r][0] = x.x;
+            v[jj][r][1] = x.y;
+          }
         }
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[e], acc[r][e]);
-      }
+      for (int jj = 0; jj < kJ; ++jj)
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+          // 0 for absent parts and rows, and for rows no merged part sees a key of
+          // (a verify row whose group holds only keys past its position)
+          const float w = mm[r] == -INFINITY ? 0.f : exp2f(mj[jj][r] - mm[r]);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[jj][r][e], acc[r][e]);
+        }
     }
     __syncwarp();
 #pragma unroll

@@ -65,6 +65,24 @@ def test_verify_block_sizes(block_size):
         run_verify(w, 4, splits)
 
 
+@pytest.mark.parametrize("group", [2, 4])
+def test_verify_split_part_that_sees_no_key(group):
+    # context 1153 in 9 fixed parts of 144 tokens: the last part is token 1152 alone, a
+    # merge group of its own, and query rows 0-2 (positions 1149-1151) see none of its
+    # keys, so that group's maxima for those rows are -inf
+    lens = [1153, 300, 1153]
+    bs = 16
+    nb = sum(-(-n // bs) for n in lens) + 3
+    perm = np.random.default_rng(12).permutation(nb).tolist()
+    tables, pos = [], 0
+    for n in lens:
+        k = -(-n // bs)
+        tables.append(perm[pos:pos + k])
+        pos += k
+    w = wl.DecodeWorkload("lone-last-part", 13, 4 * group, 4, 128, bs, nb, torch.bfloat16, lens, tables)
+    run_verify(w, 4, num_splits=9)
+
+
 def test_verify_batch256_q4_full_size_sampled():
     # the bench's verify case at full size (batch 256, one layer, q_len 4) in the launch it times;
     # the longest, the shortest and six random sequences are checked against the oracle one by one
