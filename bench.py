@@ -315,14 +315,36 @@ def bench_e2e(args, res, device, world):
     h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + list(h_meta.values()))
     d2h = sum(t.numel() * t.element_size() for t in h_out)
 
+    # Host copies overlap the kernels, as a serving loop would run them: layer l's inputs go up on
+    # one copy stream while earlier layers compute, and its output comes down on another while
+    # later layers compute.  Every step still moves all its inputs in and all its outputs out.
+    compute = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    pkv = st.pkv
+
     def one():
-        for dst, src in zip(d_q + d_k + d_v, h_q + h_k + h_v):
-            dst.copy_(src, non_blocking=True)
-        for key in h_meta:
-            d_meta[key].copy_(h_meta[key], non_blocking=True)
-        st.step(q=d_q, k_new=d_k, v_new=d_v, meta=d_meta, out=st.out)
-        for dst, src in zip(h_out, st.out):
-            dst.copy_(src, non_blocking=True)
+        up.wait_stream(compute)  # the previous step no longer reads the device inputs
+        ready = []
+        with torch.cuda.stream(up):
+            for key in h_meta:
+                d_meta[key].copy_(h_meta[key], non_blocking=True)
+            for layer in range(L):
+                for dst, src in ((d_q[layer], h_q[layer]), (d_k[layer], h_k[layer]), (d_v[layer], h_v[layer])):
+                    dst.copy_(src, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up)
+                ready.append(ev)
+        for layer in range(L):
+            compute.wait_event(ready[layer])
+            pkv.kv_store(d_k[layer], d_v[layer], st.k_cache[layer], st.v_cache[layer], d_meta["slot_mapping"])
+            pkv.paged_decode_attn(d_q[layer], st.k_cache[layer], st.v_cache[layer], d_meta["block_tables"],
+                                  d_meta["context_lens"], w.scale, workspace=st.ws, out=st.out[layer])
+            done = torch.cuda.Event()
+            done.record(compute)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                h_out[layer].copy_(st.out[layer], non_blocking=True)
+        compute.wait_stream(down)  # the step ends when its last output is on the host
 
     for _ in range(args.warmup):
         one()
