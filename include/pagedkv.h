@@ -179,8 +179,8 @@ int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const v
  *                   pkv_paged_decode_workspace_bytes(batch, q_len * num_q_heads,
  *                   head_dim, num_splits)
  *   other arguments as for paged_decode_attn.
- * Supported: BF16, head_dim 128, G in {1, 2, 4, 8} with G * q_len <= 8,
- * num_kv_heads in [1, 8].
+ * Supported: BF16, head_dim 128, G in {1, 2, 4, 8}, q_len <= 8 with
+ * G * q_len <= 16, num_kv_heads in [1, 8].
  */
 int pkv_paged_verify_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -92,8 +92,8 @@ def test_mma_kernel_stage_layouts(kv_heads, block_size, splits):
 
 # Many parts per sequence: the parts merge in groups of 8 (the last arrival of a
 # group merges it), then the last group merger merges the groups.  Covers one
-# group, a partial last group, and ~150 automatic parts; G = 2 runs the CUDA-core
-# kernel, G = 4 the tensor-core kernel.
+# group, a partial last group, and ~150 automatic parts; the fp32 case runs the
+# CUDA-core kernel, the bf16 one the tensor-core kernel.
 @pytest.mark.parametrize("group,dtype", [(2, torch.float32), (4, torch.bfloat16)])
 @pytest.mark.parametrize("lens,splits", [([60000], 0), ([20000, 3, 40000], 0), ([9000, 700], 9), ([5000], 8),
                                          ([30000, 1], 23)])
