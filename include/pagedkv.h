@@ -237,7 +237,7 @@ int pkv_kv_store_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
  *   q, out          device, bf16 [batch, num_q_heads, head_dim]
  *   k_cache,v_cache device, E4M3 bytes, layout as above
  *   workspace       as for pkv_paged_decode_attn (same size function)
- * Supported: head_dim 128; G in {1, 2, 4}; num_kv_heads in [1, 8].
+ * Supported: head_dim 128; G in {1, 2, 4, 8}; num_kv_heads in [1, 8].
  */
 int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -119,7 +119,7 @@ extern "C" int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k
   if (!(k_scale > 0.f) || !(v_scale > 0.f) || isinf(k_scale) || isinf(v_scale)) return PKV_EINVAL;
   if (head_dim != 128 || num_kv_heads > 8) return PKV_EUNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
-  if (group != 1 && group != 2 && group != 4) return PKV_EUNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_EUNSUPPORTED;
   if (static_cast<long long>(max_blocks_per_seq) * block_size > INT32_MAX) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_EINVAL;
@@ -162,6 +162,7 @@ extern "C" int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k
   switch (group) {
     case 1: return launch_fp8<1>(p, info.sms, stream);
     case 2: return launch_fp8<2>(p, info.sms, stream);
-    default: return launch_fp8<4>(p, info.sms, stream);
+    case 4: return launch_fp8<4>(p, info.sms, stream);
+    default: return launch_fp8<8>(p, info.sms, stream);
   }
 }

@@ -45,7 +45,7 @@ def _quantized_pool(shape, gen, scale):
     return torch.from_numpy(of8.quantize(as_np(x), scale))
 
 
-@pytest.mark.parametrize("group", [1, 2, 4])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
 @pytest.mark.parametrize("splits", [0, 1, 5])
 def test_fp8_decode_matches_oracle_on_dequantized_cache(group, splits):
     _fp8_decode_case(group, splits, 1.0)
@@ -144,5 +144,5 @@ def test_fp8_argument_errors():
     with pytest.raises(_lib.PagedKVError):
         pkv.paged_decode_attn_fp8(q, kc, kc, bt, cl, 0.1, 0.0, 1.0)  # scale must be > 0
     with pytest.raises(_lib.PagedKVError):
-        pkv.paged_decode_attn_fp8(torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda"), kc, kc, bt, cl, 0.1,
-                                  1.0, 1.0)  # G = 8 is not built for FP8
+        pkv.paged_decode_attn_fp8(torch.zeros(1, 6, 128, dtype=torch.bfloat16, device="cuda"), kc, kc, bt, cl, 0.1,
+                                  1.0, 1.0)  # G = 6 is not a supported group size
