@@ -238,15 +238,18 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
 // workspace slots first + i * step.  With `final` the normalized rows go to the
 // output; otherwise the merged state is written over slot `first` (each row is
 // read and written by one warp only, so the in-place write is safe).  A warp
-// takes four rows at a time so their loads overlap: one pass over the parts
-// folds each lane's share of (m, l) online and the lanes combine them by
-// shuffles; a second pass sums the weighted rows, each lane owning D / 32
-// columns, eight parts per step.
+// takes two rows at a time (so a 16-row sequence keeps all eight consumer
+// warps busy), each lane owning D / 32 columns, and folds the
+// parts in order in one pass: the running maximum m, the sum l and the
+// weighted row are rescaled whenever a part raises m (every lane keeps the
+// same m and l).  Parts are loaded kJ at a time, every load of a batch issued
+// before the first is used, so a batch costs one round trip to L2.
 template <typename T, int D>
 __device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg, int rows_per_seq, int first,
                                             int step, int count, bool final, int nthreads_c) {
-  constexpr int RW = 4;  // rows a warp merges together
+  constexpr int RW = 2;  // rows a warp merges together
   constexpr int PER = D / 32;
+  constexpr int kJ = 4;
   const int tid = threadIdx.x;
   const int warp = tid / 32;
   const int lane = tid % 32;
@@ -257,59 +260,27 @@ __device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg,
   float* ml_base = p.part_ml + static_cast<size_t>(first) * rows_per_seq * 2;
   float* o_base = p.part_o + static_cast<size_t>(first) * rows_per_seq * D + lane * PER;
   for (int row0 = warp * RW; row0 < rows_per_seq; row0 += nwarps * RW) {
-    float mm[RW], ll[RW];
+    float mm[RW], ll[RW], acc[RW][PER];
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
       mm[r] = -INFINITY;
       ll[r] = 0.f;
-    }
-    // (m, l) of this lane's parts, folded online
-    for (int j = lane; j < count; j += 32) {
-#pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        if (row0 + r >= rows_per_seq) continue;
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(ml_base + j * ml_stride + (row0 + r) * 2));
-        const float mn = fmaxf(mm[r], v.x);
-        if (mn != -INFINITY) {
-          ll[r] = ll[r] * exp2f(mm[r] - mn) + v.y * exp2f(v.x - mn);
-          mm[r] = mn;
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < RW; ++r) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, mm[r], off);
-        const float lo = __shfl_xor_sync(0xffffffffu, ll[r], off);
-        const float mn = fmaxf(mm[r], mo);
-        if (mn != -INFINITY) {
-          ll[r] = ll[r] * exp2f(mm[r] - mn) + lo * exp2f(mo - mn);
-          mm[r] = mn;
-        }
-      }
-    }
-    float acc[RW][PER];
-#pragma unroll
-    for (int r = 0; r < RW; ++r)
 #pragma unroll
       for (int e = 0; e < PER; ++e) acc[r][e] = 0.f;
-    // kJ parts at a time: every load of a batch is issued before the first is
-    // used, so a batch costs one round trip to L2
-    constexpr int kJ = 4;
+    }
     for (int j0 = 0; j0 < count; j0 += kJ) {
       float v[kJ][RW][PER];
-      float mj[kJ][RW];
+      float2 ml[kJ][RW];
 #pragma unroll
       for (int jj = 0; jj < kJ; ++jj)
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
-          mj[jj][r] = -INFINITY;
+          ml[jj][r] = make_float2(-INFINITY, 0.f);
 #pragma unroll
           for (int e = 0; e < PER; ++e) v[jj][r][e] = 0.f;
           if (j0 + jj >= count || row0 + r >= rows_per_seq) continue;
           const size_t j = j0 + jj;
-          mj[jj][r] = __ldcg(ml_base + j * ml_stride + (row0 + r) * 2);
+          ml[jj][r] = __ldcg(reinterpret_cast<const float2*>(ml_base + j * ml_stride + (row0 + r) * 2));
           const float* src = o_base + j * o_stride + static_cast<size_t>(row0 + r) * D;
           if constexpr (PER == 4) {
             const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
@@ -327,11 +298,18 @@ __device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg,
       for (int jj = 0; jj < kJ; ++jj)
 #pragma unroll
         for (int r = 0; r < RW; ++r) {
-          // 0 for absent parts and rows, and for rows no merged part sees a key of
-          // (a verify row whose group holds only keys past its position)
-          const float w = mm[r] == -INFINITY ? 0.f : exp2f(mj[jj][r] - mm[r]);
+          const float mn = fmaxf(mm[r], ml[jj][r].x);
+          // absent parts and rows, and parts that saw no key of this row (a
+          // verify row whose part holds only keys past its position), carry
+          // m = -inf: they add nothing, and a row none of whose parts saw a
+          // key keeps m = -inf, l = 0 and a zero row
+          if (mn == -INFINITY) continue;
+          const float a = exp2f(mm[r] - mn);
+          const float w = exp2f(ml[jj][r].x - mn);
+          ll[r] = fmaf(ll[r], a, ml[jj][r].y * w);
 #pragma unroll
-          for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(w, v[jj][r][e], acc[r][e]);
+          for (int e = 0; e < PER; ++e) acc[r][e] = fmaf(acc[r][e], a, w * v[jj][r][e]);
+          mm[r] = mn;
         }
     }
     __syncwarp();
