@@ -1,6 +1,7 @@
-// Device helpers shared by the paged KV-cache kernels: mbarrier pipeline
-// primitives with bounded waits, 1-D bulk (TMA) copies, bf16 unpacking and
-// the per-device error word.
+// Helpers shared by the paged KV-cache kernels: mbarrier pipeline primitives
+// with bounded waits, 1-D bulk (TMA) copies and tensor-map encoding,
+// programmatic dependent launch, mma.sync / ldmatrix wrappers, bf16 and E4M3
+// unpacking, and the per-device error word.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -33,9 +34,9 @@ int encode_bf16_3d(void* map, const void* base, uint64_t d0, uint64_t d1, uint64
 
 // Encodes the 4-D tensor map of one paged K or V pool [num_blocks,
 // block_size, hkv, 128] whose box is 16 tokens of every KV head and 128 bytes
-// of head_dim, ordered (head, token) in shared memory with 128-byte swizzle: rows of one head's 16 tokens are 128 bytes apart, so any
-// eight consecutive tokens fill the eight swizzle phases.  block_size must be a
-// multiple of 16.
+// of head_dim, ordered (head, token) in shared memory with 128-byte swizzle:
+// rows of one head's 16 tokens are 128 bytes apart, so any eight consecutive
+// tokens fill the eight swizzle phases.  block_size must be a multiple of 16.
 // elem_bytes: 2 (bf16, box of 64 elements, two copies per 16-token box) or 1
 // (E4M3 codes, box of 128, one copy).
 int encode_paged_kv(void* map, const void* base, uint32_t block_size, uint32_t hkv, uint64_t num_blocks,

@@ -8,23 +8,24 @@
 // with K_t / V_t at physical block block_tables[b, t / bs], offset t % bs.
 // context_lens 0 writes zeros and reads nothing.
 //
-// How (GB300 design):
+// How (GB300 design; the kernels are in decode_kernel.cuh and the files it
+// includes):
 //  * A CTA covers every KV head of a token range, so each token's K (or V)
 //    row of all heads, [Hkv, D], is contiguous in the [blocks, bs, Hkv, D]
-//    pool and a run of tokens inside one block is one contiguous span.  One
-//    producer lane streams those spans into a ring of shared-memory stages with
-//    1-D bulk (TMA) copies completed on mbarriers; every K/V byte is read from
-//    HBM exactly once, and all G query heads of a KV head reuse it on chip.
-//  * One consumer warp per (KV head, token phase).  Within a warp LPT lanes
-//    share a token (16-byte conflict-free shared loads, fp32 dot products,
-//    xor-shuffle reduction); scores of a stage are reduced to a stage maximum
-//    and folded into a running online softmax (exp2 domain), then P.V is
-//    accumulated in registers.
+//    pool.  A producer warp streams the range into a ring of shared-memory
+//    stages with TMA copies completed on mbarriers; every K/V byte is read
+//    from HBM once, and all G query heads of a KV head reuse it on chip.
+//  * bf16 caches with head_dim 128 run on paged_decode_mma_kernel: each
+//    consumer warp takes 16-token chunks and computes S = Q K^T and
+//    O^T = V^T P^T with mma.sync, with an online softmax in the exp2 domain on
+//    the accumulator fragments.  fp32 caches and head_dim 64 run on
+//    paged_decode_kernel (CUDA-core dot products and shuffle reductions).
 //  * Split over the context: the batch's context tokens, flattened, are
-//    divided evenly over the grid (automatic mode) or each sequence into S
-//    equal parts.  A sequence covered by one CTA is written directly; otherwise
-//    each part writes (o, m, l) to the workspace and the last CTA to finish
-//    a sequence (atomic ticket, no waiting) merges the parts by log-sum-exp.
+//    divided evenly over one persistent CTA per SM (automatic mode) or each
+//    sequence into S equal parts.  A sequence covered by one CTA is written
+//    directly; otherwise each part writes (o, m, l) to the workspace and
+//    atomic tickets (no waiting) elect the CTAs that merge the parts by
+//    log-sum-exp, in groups of eight consecutive parts and then the groups.
 #include "decode_kernel.cuh"
 
 extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
