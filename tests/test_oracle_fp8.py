@@ -50,3 +50,23 @@ def test_quantize_divides_in_float32():
     x = np.float32(3.0)
     assert fp8.quantize(x, 0.1) == fp8.e4m3_encode(np.float64(np.float32(3.0) / np.float32(0.1)))
     assert fp8.dequantize(fp8.quantize(np.float32(1.0), 0.5), 0.5) == 1.0
+
+
+def test_quantize_rounds_the_float32_quotient():
+    # The store divides in float32 (the kernel's input precision).  For these
+    # inputs the float32 quotient x / scale lands exactly on the midpoint
+    # between two E4M3 values while the exact quotient lies just above it, so
+    # the stored code must be the midpoint's even neighbour.  Expected codes
+    # come from numpy's IEEE float32 division and torch's float8 conversion.
+    found = 0
+    for mid in (1.0625, 2.125, 17.0):  # midpoints of (1, 1.125), (2, 2.25), (16, 18)
+        for k in range(200):
+            s = np.float32(0.1 + 0.00037 * k)
+            x = np.float32(mid * float(s))
+            q32 = x / s
+            if q32 != np.float32(mid) or not float(x) / float(s) > mid:
+                continue
+            want = torch.tensor(float(q32), dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).item()
+            assert fp8.quantize(x, float(s)) == want
+            found += 1
+    assert found >= 10
