@@ -26,6 +26,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")  # the CPU oracle runs on one core; its line says so
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -99,19 +100,22 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons; the summary keeps
+    the samples stamped inside the timed region (mark() before it, mark() after it)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int):
         self.proc = None
+        self.marks = []
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         sel = self._selector(device_index)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"] + sel, stdout=self.file, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"] + sel, stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -131,10 +135,14 @@ class ClockSampler:
             return ["-i", vis.split(",")[device_index]]
         return ["-i", str(device_index)]
 
+    def mark(self) -> None:
+        """Host wall-clock time of the start (first call) or end (second call) of the timed region."""
+        self.marks.append(time.time())
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -142,24 +150,39 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        text = self.file.read()
         os.unlink(self.file.name)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 8:
+        window = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else None
+        return self.summarise(text, window)
+
+    @classmethod
+    def summarise(cls, text: str, window) -> dict:
+        """Median SM clock, max clock and active throttle reasons of the samples stamped within
+        `window` (host seconds, widened by one 50 ms interval); all samples if none fall inside."""
+        rows = []
+        for line in text.strip().splitlines():
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 9:
                 continue
             try:
-                sm.append(float(r[0]))
-                smax.append(float(r[1]))
+                stamp = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                stamp = None
+            try:
+                rows.append((stamp, float(r[1]), float(r[2]), r[5:9]))
             except ValueError:
                 continue
-            for name, val in zip(names, r[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = rows
+        scope = "all samples"
+        if window is not None:
+            lo, hi = window[0] - 0.05, window[1] + 0.05
+            sel = [r for r in rows if r[0] is not None and lo <= r[0] <= hi]
+            if sel:
+                inside, scope = sel, "timed region"
+        reasons = {name for r in inside for name, val in zip(cls.REASONS, r[3]) if val.lower() == "active"}
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "samples": len(inside), "window": scope, "reasons": sorted(reasons)}
 
 
 DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh",
@@ -280,6 +303,7 @@ def bench_decode(args, device, world):
     sampler = ClockSampler(device.index or 0)
     barrier(world)
     torch.cuda.synchronize()
+    sampler.mark()
     torch.cuda.nvtx.range_push("timed_steps")
     start.record()
     for k in range(args.steps):
@@ -287,6 +311,7 @@ def bench_decode(args, device, world):
     stop.record()
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    sampler.mark()
     barrier(world)
     clocks = sampler.stop()
     ms_total = max_over_ranks(start.elapsed_time(stop), world, device)
