@@ -195,3 +195,31 @@ def test_out_of_range_indices_raise_device_error_bits():
     pkv.paged_decode_attn(q, kc, kc, bt, torch.tensor([17], dtype=torch.int32, device=dev), 0.1, num_splits=1)
     assert pkv.device_error() & _lib.DERR_LEN_RANGE
     assert pkv.device_error() == 0
+
+
+@pytest.mark.gpu
+def test_binding_rejects_mismatched_shapes_before_launch():
+    # a wrong-sized out or a cache of another head_dim would make a kernel write or read
+    # out of bounds: the binding refuses them on the host
+    dev = "cuda"
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(2, 3, dtype=torch.int32, device=dev)
+    cl = torch.ones(2, dtype=torch.int32, device=dev)
+    short = torch.empty(1, 4, 128, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError, match="out must have shape"):
+        pkv.paged_decode_attn(q, kc, kc, bt, cl, 0.1, num_splits=1, out=short)
+    with pytest.raises(ValueError, match="out must have shape"):
+        pkv.paged_decode_attn_noalloc(q, kc, kc, bt, cl, 0.1, out=short)
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        pkv.paged_decode_attn_noalloc(q, kc[..., :64].contiguous(), kc[..., :64].contiguous(), bt, cl, 0.1)
+    with pytest.raises(ValueError, match="out must have shape"):
+        pkv.paged_verify_attn(q[:, None], kc, kc, bt, cl, 0.1, num_splits=1, out=short)
+    cu = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    with pytest.raises(ValueError, match="head_dim differs"):
+        pkv.paged_varlen_prefill_attn(q[:1], cu, cu, 1, 1, 0.1, k_cache=kc[..., :64].contiguous(),
+                                      v_cache=kc[..., :64].contiguous(), block_tables=bt[:1])
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        pkv.paged_decode_attn(q, kc, kc, bt.cpu(), cl, 0.1, num_splits=1)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
