@@ -15,12 +15,16 @@ from .ops import (  # noqa: F401
     kv_store_fp8,
     paged_decode_attn,
     paged_decode_attn_fp8,
+    paged_decode_attn_noalloc,
     paged_varlen_prefill_attn,
     paged_verify_attn,
     prefill_workspace,
     prefill_workspace_bytes,
 )
 
-__all__ = ["copy_blocks", "kv_store", "kv_store_fp8", "paged_decode_attn", "paged_decode_attn_fp8", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
-           "decode_workspace_bytes", "prefill_workspace", "prefill_workspace_bytes", "device_error", "metadata", "ops",
-           "workloads"]
+__all__ = [
+    "copy_blocks", "kv_store", "kv_store_fp8", "paged_decode_attn", "paged_decode_attn_fp8",
+    "paged_decode_attn_noalloc", "paged_varlen_prefill_attn", "paged_verify_attn", "decode_workspace",
+    "decode_workspace_bytes", "prefill_workspace", "prefill_workspace_bytes", "device_error", "metadata", "ops",
+    "workloads",
+]
