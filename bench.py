@@ -8,10 +8,19 @@ each layer, kv_store of the step's new token then paged decode attention.
 Inputs total ~139 GB, far larger than L2, so no flush is needed between steps.
 
 Printed (one JSON line, rank 0):
-  value       algorithmic HBM bytes of the whole step (store + decode, 28 layers) / step time, GB/s
-  roofline    the dominant kernel (paged decode) against the measured HBM copy peak
-  e2e         the same metric through the public API with host buffers (H2D inputs, D2H outputs)
-  prefill     the varlen prefill row on a 16-sequence prefix-cached chunked batch, TFLOP/s
+  value        algorithmic HBM bytes of the whole step (store + decode, 28 layers) / step time, GB/s
+  roofline     the dominant kernel (paged decode) against the measured HBM copy peak, with its
+               ncu DRAM traffic per launch while the decode sources match the recorded capture
+  e2e          the same metric through the public API with host buffers (H2D inputs, D2H outputs)
+  clocks       nvidia-smi SM clock and throttle reasons sampled inside the timed region
+  gpu_launches this library's kernel launches inside the timed region
+  prefill, prefill_long_history
+               the varlen prefill row (16-sequence prefix-cached chunked batch; one sequence
+               with a 16k-token history), TFLOP/s against the measured bf16 peak
+  long_context, verify, kv_store, copy_blocks, cuda_graph_decode, fp8_kv
+               the other rows: long-context split decode, speculative verify (q_len 4), the
+               store alone, copy-on-write block copies, the batch-8 step replayed as a CUDA
+               graph, and the step over an E4M3 cache
   cpu_baseline the CPU oracle timed on a bounded sample of the same workload
 
 ``--impl reference`` times the CPU oracle itself on bounded samples of the
