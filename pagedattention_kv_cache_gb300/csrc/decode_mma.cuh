@@ -9,16 +9,18 @@ namespace {
 
 // ------------------------------------------------------------------ tensor-core variant
 //
-// With R >= 3 rows per KV head (grouped-query heads x verify tokens) the
+// Past R = 2 rows per KV head (grouped-query heads x verify tokens) the
 // CUDA-core loop of decode_simt.cuh runs out of registers and issue slots
-// before HBM is saturated.  This variant keeps the same CTA plan, producer, split and
-// combine, but each consumer warp computes its 16-token chunk of a stage with
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate): S = Q K^T with the R rows in
-// the M dimension (rows >= R are zero), online softmax on the accumulator
-// fragments (O rescaled only when a row maximum grows by more than 2^8), and
-// O += P V with P taken straight from the S fragments.  The eight keys an
-// ldmatrix reads must sit in eight different bank groups; two stage layouts
-// give that:
+// before HBM is saturated; with the layouts below this kernel is also the
+// faster one at R = 1 and 2, so it runs every bf16 or FP8 cache with
+// head_dim 128.  It keeps the same CTA plan, split and merge, but each
+// consumer warp computes its 16-token chunks of a stage with mma.sync
+// m16n8k16 (fp32 accumulate): S = Q K^T with the R rows in the M dimension
+// (rows >= R are zero), online softmax on the accumulator fragments (O
+// rescaled only when a row maximum grows by more than 2^8), and P V with P
+// taken straight from the S fragments (as O^T = V^T P^T when R <= 8).  The
+// eight keys an ldmatrix reads must sit in eight different bank groups; two
+// stage layouts give that:
 //  * block_size a multiple of 16 (p.tma): a warp's 16 keys lie in one block,
 //    and four tensor copies (K and V, two halves of head_dim) of a 16-token box
 //    of every KV head fill its chunk, 128-byte swizzled, rows of one head's
@@ -47,13 +49,14 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
 //    m16n8k16 step is permuted that way on both operands, so Q's fragments are
 //    loaded in the same order.  Q is f16 after a per-row power-of-two scaling
 //    that puts its largest element in [2^14, 2^15).
-//  * O += P V: P is f16 times 2^7 (the lazy rescale lets P reach 2^8, and
-//    2^15 is f16's top binade); l sums the same rounded weights, so the
-//    factor cancels.  V's B fragment
-//    pairs two keys of one column, so each lane reads 16 consecutive codes of
-//    four key rows and byte-permutes key pairs together; n-tile j, column n
-//    then stands for head_dim index 16 n + j, and a lane's accumulators cover
-//    32 consecutive outputs.
+//  * O^T += V^T P^T (an FP8 cache always has R <= 8): P is f16 times 2^7 (the
+//    lazy rescale lets P reach 2^8, and 2^15 is f16's top binade); l sums the
+//    same rounded weights, so the factor cancels.  V^T's A fragment pairs two
+//    keys of one head_dim index, which ldmatrix.trans cannot form from bytes:
+//    each lane reads 16 consecutive codes of four key rows and byte-permutes
+//    key pairs together.  m-tile t, row m then stands for head_dim index
+//    16 m + 2t (m < 8) or 16 (m - 8) + 2t + 1, and a lane's accumulators cover
+//    16 consecutive outputs of each of its two rows.
 // 16-key chunks a consumer warp takes per stage: two for an FP8 cache (its
 // stages hold twice the tokens in the same bytes, and the second chunk's
 // scores overlap the first's latency), one for bf16.

@@ -239,11 +239,11 @@ __device__ __forceinline__ bool for_each_segment(const Params& p, const Plan& pl
 // output; otherwise the merged state is written over slot `first` (each row is
 // read and written by one warp only, so the in-place write is safe).  A warp
 // takes two rows at a time (so a 16-row sequence keeps all eight consumer
-// warps busy), each lane owning D / 32 columns, and folds the
-// parts in order in one pass: the running maximum m, the sum l and the
-// weighted row are rescaled whenever a part raises m (every lane keeps the
-// same m and l).  Parts are loaded kJ at a time, every load of a batch issued
-// before the first is used, so a batch costs one round trip to L2.
+// warps busy), each lane owning D / 32 columns, and folds the parts in order
+// in one pass: the running maximum m, the sum l and the weighted row are
+// rescaled whenever a part raises m (every lane keeps the same m and l).
+// Parts are loaded kJ at a time, every load of a batch issued before the
+// first is used, so a batch costs one round trip to L2.
 template <typename T, int D>
 __device__ __forceinline__ void merge_parts(const Params& p, const Segment& seg, int rows_per_seq, int first,
                                             int step, int count, bool final, int nthreads_c) {
