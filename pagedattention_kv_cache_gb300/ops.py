@@ -1,8 +1,10 @@
 """Python binding of the C ABI: argument marshalling only.
 
 Each function takes torch tensors that already live on the current CUDA
-device, checks dtype / shape / contiguity, and passes raw pointers and sizes
-to libpagedkv.so on the current torch stream.  Every step of the path runs
+device, checks device, dtype, shape and contiguity (a mismatch that would let
+a kernel read or write out of bounds is a host-side error, raised before any
+launch), and passes raw pointers and sizes to libpagedkv.so on the current
+torch stream.  Every step of the path runs
 in the library's CUDA kernels; nothing here computes.
 """
 
