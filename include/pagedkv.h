@@ -283,7 +283,7 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
 
 /*
  * paged_varlen_prefill_attn: sequence i owns query rows cu_seqlens_q[i] ..
- * cu_seqlens_q[i+1]-1 (nq rows, the tokens computed this round) and nk =
+ * cu_seqlens_q[i+1]-1 (nq rows, the tokens computed in this scheduler step) and nk =
  * cu_seqlens_k[i+1] - cu_seqlens_k[i] keys; the first c = nk - nq keys are
  * history.  Query row r is at absolute position c + r and, when causal, attends
  * keys 0 .. c + r (bottom-right aligned); otherwise all nk keys.

@@ -166,7 +166,7 @@ def paged_prefill_attention(q, cu_seqlens_q, cu_seqlens_k, scale: float, *, k_ca
     """Varlen (packed) prefill / chunked-prefill attention.
 
     "3.6 ModelRunner ...", section 2: sequence i owns query rows
-    cu_seqlens_q[i]..cu_seqlens_q[i+1]-1 (the tokens computed this round) and
+    cu_seqlens_q[i]..cu_seqlens_q[i+1]-1 (the tokens computed in this scheduler step) and
     its keys span positions 0..nk-1 with nk = cu_seqlens_k[i+1] - cu_seqlens_k[i].
     The first c = nk - nq keys are history (prefix-cache hit or an earlier
     chunk); query row r sits at absolute position c + r and, when causal,

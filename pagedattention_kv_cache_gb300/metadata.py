@@ -27,8 +27,8 @@ def prefill_metadata(block_tables: list[list[int]], num_cached: list[int], num_n
     """slot_mapping / cu_seqlens_q / cu_seqlens_k / max_seqlen_* / block_tables for a packed prefill.
 
     Tokens [num_cached[i], num_cached[i] + num_new[i]) of sequence i are
-    computed this round; the K side runs from 0.  block_tables is None when
-    no sequence has history (then the kernel reads this round's k, v), unless
+    computed in this scheduler step; the K side runs from 0.  block_tables is None when
+    no sequence has history (then the kernel reads this step's k, v), unless
     ``always_tables`` asks for it anyway (attention then reads the stored rows).
     """
     cached = np.asarray(num_cached, dtype=np.int64)

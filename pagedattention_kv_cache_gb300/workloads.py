@@ -71,7 +71,7 @@ class PrefillWorkload:
     num_blocks: int
     dtype: torch.dtype
     num_cached: list[int]  # tokens already in the cache per sequence (prefix hit / earlier chunks)
-    num_new: list[int]  # tokens computed this round per sequence
+    num_new: list[int]  # tokens computed in this scheduler step per sequence
     block_tables: list[list[int]]  # covers num_cached + num_new tokens
 
     @property
@@ -165,7 +165,7 @@ def random_decode(seed: int, *, batch: int, max_ctx: int, block_size: int, num_q
 
 def qwen3_prefill_prefix(seed: int = 1004, batch: int = 16, chunk: int = 512) -> PrefillWorkload:
     """16 sequences of total length uniform in [256, 4096]; a random multiple of the block size
-    (0 to half the length) is already cached; up to ``chunk`` new tokens per sequence this round."""
+    (0 to half the length) is already cached; up to ``chunk`` new tokens per sequence in this step."""
     rng = np.random.default_rng(seed)
     bs = 256
     lens = rng.integers(256, 4096, size=batch, endpoint=True).tolist()
@@ -260,7 +260,7 @@ def decode_tensors(wl: DecodeWorkload, device="cpu", layer: int = 0, poison: boo
 
 
 def prefill_tensors(wl: PrefillWorkload, device="cpu", poison: bool = False) -> dict:
-    """Draw q / k / v for this round's tokens (packed [total_q, H, D]) and the cache pools.
+    """Draw q / k / v for this step's tokens (packed [total_q, H, D]) and the cache pools.
 
     The cache holds N(0, 1) history for every sequence's cached prefix; the
     new rows k, v are to be stored through slot_mapping before attention.

@@ -90,7 +90,7 @@ def run_decode(w: wl.DecodeWorkload, *, num_splits: int = 0, poison: bool = Fals
 
 def run_prefill(w: wl.PrefillWorkload, *, use_tables: bool = True, poison: bool = False, device="cuda",
                 causal: bool = True, workspace=None) -> dict:
-    """Store this round's rows and run varlen prefill on the GPU; compare with the oracle."""
+    """Store this step's rows and run varlen prefill on the GPU; compare with the oracle."""
     t = wl.prefill_tensors(w, "cpu", poison=poison)
     meta = md.prefill_metadata(w.block_tables, w.num_cached, w.num_new, w.block_size, always_tables=use_tables)
     g = {k: v.to(device, copy=True) for k, v in t.items()}

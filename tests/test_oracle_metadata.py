@@ -39,7 +39,7 @@ def test_worked_example_prefill_matches_page():
 
 
 def test_no_history_needs_no_block_tables():
-    # Q and K the same length: the kernel uses this round's k/v directly (section 2)
+    # Q and K the same length: the kernel uses this step's k/v directly (section 2)
     seqs = [dict(block_table=[3, 1], num_cached_tokens=0, num_scheduled_tokens=6),
             dict(block_table=[0], num_cached_tokens=0, num_scheduled_tokens=2)]
     md = om.prepare_prefill(seqs, 4)
