@@ -264,7 +264,9 @@ int pkv_paged_decode_attn_fp8(void* out, const void* q, const void* k_cache, con
  * loads the library until the process exits.  Sizes whose workspace
  * (pkv_paged_decode_workspace_bytes) exceeds it return PKV_ESCRATCH without
  * launching; with 152 SMs, 16 query heads and head_dim 128 the automatic
- * split fits batches up to about 700.
+ * split fits batches up to about 700.  Every argument is checked first, as
+ * for pkv_paged_decode_attn: a call that returns an error has queued nothing
+ * on `stream`.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
@@ -296,10 +298,12 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *   q               device, [total_q, num_q_heads, head_dim]
  *   k, v            device, [total_k, num_kv_heads, head_dim]; read only when block_tables == NULL
  *   k_cache,v_cache device, cache layout above; read only when block_tables != NULL
- *   cu_seqlens_q/k  device, int32 [batch + 1], non-decreasing, starting at 0; every
- *                   nk >= nq, cu_seqlens_q[batch] <= total_q and, without block_tables,
- *                   cu_seqlens_k[batch] <= total_k (a sequence breaking these is skipped
- *                   and raises PKV_DERR_LEN_RANGE)
+ *   cu_seqlens_q/k  device, int32 [batch + 1], non-decreasing, starting at 0.  A
+ *                   sequence whose rows fall outside q / out (cu_seqlens_q[i] < 0 or
+ *                   cu_seqlens_q[i+1] > total_q), with nq < 0 or nk < nq, with nq >
+ *                   max_seqlen_q, with more keys than its table row covers, or, without
+ *                   block_tables, with key rows outside [0, total_k), is skipped (its
+ *                   output rows are not written) and raises PKV_DERR_LEN_RANGE
  *   max_seqlen_q    >= every nq (sizes the grid); max_seqlen_k >= every nk
  *   block_tables    device, int32 [batch, max_blocks_per_seq] or NULL
  *   total_q, total_k rows of q/out and of the packed k/v (total_k is ignored with block_tables)

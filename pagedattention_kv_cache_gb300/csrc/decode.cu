@@ -37,12 +37,15 @@ extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_
   return workspace_layout(batch, num_q_heads, head_dim, num_splits, info.sms, &a, &b);
 }
 
-extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                     const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
-                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                     int32_t num_blocks, float scale, int32_t num_splits, void* workspace,
-                                     size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+namespace {
+
+// Host-side argument checks of pkv_paged_decode_attn (everything but the
+// workspace): PKV_OK when a launch may follow, 1 when batch is 0 (nothing to
+// do), else the negative status to return.
+int check_decode_args(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                      int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t num_blocks, int32_t num_splits, pkv_dtype dtype) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_blocks < 0 || max_blocks_per_seq < 0 || num_splits < 0)
     return PKV_EINVAL;
@@ -51,10 +54,24 @@ extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cac
   if (head_dim != 64 && head_dim != 128) return PKV_EUNSUPPORTED;
   if (num_kv_heads > 8) return PKV_EUNSUPPORTED;
   if (static_cast<long long>(max_blocks_per_seq) * block_size > INT32_MAX) return PKV_EINVAL;
-  if (batch == 0) return PKV_OK;
+  if (batch == 0) return 1;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_EINVAL;
   if (!pkv::aligned16(out) || !pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
     return PKV_EALIGN;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     int32_t num_blocks, float scale, int32_t num_splits, void* workspace,
+                                     size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+  const int chk = check_decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                                    num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, num_splits, dtype);
+  if (chk != PKV_OK) return chk > 0 ? PKV_OK : chk;
 
   pkv::DeviceInfo info;
   if (pkv::device_info(&info) != PKV_OK) return PKV_ECUDA;
@@ -143,7 +160,11 @@ extern "C" int pkv_paged_decode_attn_noalloc(void* out, const void* q, const voi
                                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                              int32_t num_blocks, float scale, int32_t num_splits, pkv_dtype dtype,
                                              pkv_stream_t stream) {
-  if (batch < 0 || num_q_heads <= 0 || head_dim <= 0 || num_splits < 0) return PKV_EINVAL;
+  // every argument is checked before anything is queued on the stream (the
+  // memset below included)
+  const int chk = check_decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                                    num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, num_splits, dtype);
+  if (chk != PKV_OK) return chk > 0 ? PKV_OK : chk;
   pkv::DeviceInfo info;
   if (pkv::device_info(&info) != PKV_OK) return PKV_ECUDA;
   size_t off_o = 0, off_ml = 0;

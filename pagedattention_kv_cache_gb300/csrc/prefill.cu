@@ -41,6 +41,7 @@ struct Params {
   unsigned int* err;
   int total_q;
   int total_k;
+  int max_seqlen_q;
   int max_blocks;
   int batch;
   int hq;
@@ -140,12 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
   const int k_begin = __ldg(p.cu_k + seq);
   const int nk = __ldg(p.cu_k + seq + 1) - k_begin;
   const int tok0 = blockIdx.x * TQ;
-  if (tok0 >= nq) return;
-  if (nk < nq || q_begin + nq > p.total_q || (p.block_tables && nk > p.max_blocks * p.block_size) ||
-      (!p.block_tables && k_begin + nk > p.total_k)) {
+  // the same range rule as the tcgen05 kernel: rows inside q / out and the packed
+  // k / v, and at most max_seqlen_q rows (the grid's size); otherwise skipped
+  if (q_begin < 0 || nq < 0 || nk < nq || static_cast<long long>(q_begin) + nq > p.total_q || nq > p.max_seqlen_q ||
+      (p.block_tables ? static_cast<long long>(nk) > static_cast<long long>(p.max_blocks) * p.block_size
+                      : (k_begin < 0 || static_cast<long long>(k_begin) + nk > p.total_k))) {
     if (threadIdx.x == 0) pkv::raise_error(p.err, PKV_DERR_LEN_RANGE);
     return;
   }
+  if (tok0 >= nq) return;
   const int cached = nk - nq;
   const int tok_last = min(nq, tok0 + TQ) - 1;
   const int keys_needed = p.causal ? cached + tok_last + 1 : nk;
@@ -407,6 +411,7 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
   p.err = err;
   p.total_q = total_q;
   p.total_k = total_k;
+  p.max_seqlen_q = max_seqlen_q;
   p.max_blocks = max_blocks_per_seq;
   p.batch = batch;
   p.hq = num_q_heads;

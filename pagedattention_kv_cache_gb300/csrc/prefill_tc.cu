@@ -97,6 +97,7 @@ struct TcParams {
   unsigned int* err;
   int total_q;
   int total_k;
+  int max_seqlen_q;
   int max_blocks;
   int hq;
   int hkv;
@@ -215,12 +216,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int k_begin = __ldg(p.cu_k + seq);
   const int nk = __ldg(p.cu_k + seq + 1) - k_begin;
   const int tok0 = qt * TQ;
-  if (tok0 >= nq) return;
-  if (nk < nq || q_begin + nq > p.total_q || (p.paged && nk > p.max_blocks * p.block_size) ||
-      (!p.paged && k_begin + nk > p.total_k)) {
+  // cu_seqlens must describe rows inside q / out (and the packed k / v), and no
+  // sequence may have more rows than max_seqlen_q, which sized the grid: such a
+  // sequence is skipped whole and raises the range bit
+  if (q_begin < 0 || nq < 0 || nk < nq || static_cast<long long>(q_begin) + nq > p.total_q || nq > p.max_seqlen_q ||
+      (p.paged ? static_cast<long long>(nk) > static_cast<long long>(p.max_blocks) * p.block_size
+               : (k_begin < 0 || static_cast<long long>(k_begin) + nk > p.total_k))) {
     if (threadIdx.x == 0) raise_error(p.err, PKV_DERR_LEN_RANGE);
     return;
   }
+  if (tok0 >= nq) return;
   const int cached = nk - nq;
   const int tok_last = min(nq, tok0 + TQ) - 1;
   const int keys_needed = p.causal ? cached + tok_last + 1 : nk;
@@ -639,6 +644,7 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   p.err = a.err;
   p.total_q = a.total_q;
   p.total_k = a.total_k;
+  p.max_seqlen_q = a.max_seqlen_q;
   p.max_blocks = a.max_blocks;
   p.hq = a.hq;
   p.hkv = a.hkv;

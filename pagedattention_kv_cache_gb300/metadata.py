@@ -62,11 +62,25 @@ def decode_metadata(block_tables: list[list[int]], lengths: list[int], block_siz
     """slot_mapping / context_lens / block_tables for one decode step.
 
     ``lengths`` count the new token.  Its slot is at position length - 1, in
-    the last block of the table.
+    the last block of the table, so every table must hold exactly
+    ceil(length / block_size) blocks (none for a length-0 padding row): with a
+    longer table the last entry would not be the block of position length - 1.
+    A table of another length raises ValueError.
     """
+    if block_size <= 0:
+        raise ValueError("block_size must be positive")
+    if len(block_tables) != len(lengths):
+        raise ValueError("one block table per sequence is required")
     lens = np.asarray(lengths, dtype=np.int64)
-    last = np.array([t[-1] if t else -1 for t in block_tables], dtype=np.int64)
+    if lens.size and lens.min() < 0:
+        raise ValueError("lengths must be non-negative")
     n_blocks = np.array([len(t) for t in block_tables], dtype=np.int64)
+    bad = np.flatnonzero(n_blocks != -(-lens // block_size))
+    if bad.size:
+        b = int(bad[0])
+        raise ValueError(f"sequence {b}: length {int(lens[b])} needs {-(-int(lens[b]) // block_size)} blocks of "
+                         f"{block_size}, its table has {int(n_blocks[b])}")
+    last = np.array([t[-1] if t else -1 for t in block_tables], dtype=np.int64)
     in_last = lens - (n_blocks - 1) * block_size
     slots = np.where(lens > 0, last * block_size + in_last - 1, -1).astype(np.int32)
     return {

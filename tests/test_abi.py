@@ -106,6 +106,42 @@ def test_host_metadata_matches_oracle():
             assert np.array_equal(dgot[key], dwant[key]), key
 
 
+def test_decode_metadata_refuses_tables_of_the_wrong_length():
+    # the new token's slot comes from the last table entry, so the table must hold exactly
+    # ceil(length / block_size) blocks, as the oracle requires
+    assert md.decode_metadata([[3, 1], []], [6, 0], 4)["slot_mapping"].tolist() == [5, -1]
+    for tables, lens in (([[3, 1, 9]], [6]), ([[3]], [6]), ([[2]], [0]), ([[]], [1])):
+        with pytest.raises(ValueError, match="table has"):
+            md.decode_metadata(tables, lens, 4)
+        with pytest.raises(ValueError):
+            om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(tables, lens)], 4)
+    with pytest.raises(ValueError):
+        md.decode_metadata([[1]], [-1], 4)
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host():
+    # argument errors come back before any CUDA call (and so before its scratch memset is queued):
+    # these pointers are never dereferenced
+    _built()
+    lib = _lib.load()
+    f = lib.pkv_paged_decode_attn_noalloc
+    ok_ptr = 4096
+    args = dict(out=ok_ptr, q=ok_ptr, kc=ok_ptr, vc=ok_ptr, bt=ok_ptr, mb=4, cl=ok_ptr, batch=2, hq=4, hkv=2, d=128,
+                bs=16, nb=8, scale=ctypes.c_float(0.1), splits=0, dtype=_lib.BF16, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"], a["batch"], a["hq"], a["hkv"], a["d"],
+                 a["bs"], a["nb"], a["scale"], a["splits"], a["dtype"], a["stream"])
+
+    assert call(out=None) == _lib.EINVAL
+    assert call(hq=3) == _lib.EINVAL
+    assert call(d=96) == _lib.EUNSUPPORTED
+    assert call(dtype=7) == _lib.EUNSUPPORTED
+    assert call(q=ok_ptr + 8) == _lib.EALIGN
+    assert call(batch=0) == _lib.OK
+
+
 def test_pad_decode_rows():
     m = md.pad_decode(md.decode_metadata([[3, 1]], [6], 4), 4)
     assert m["slot_mapping"].tolist() == [5, -1, -1, -1]
@@ -194,6 +230,35 @@ def test_out_of_range_indices_raise_device_error_bits():
     assert pkv.device_error() & _lib.DERR_BLOCK_RANGE
     pkv.paged_decode_attn(q, kc, kc, bt, torch.tensor([17], dtype=torch.int32, device=dev), 0.1, num_splits=1)
     assert pkv.device_error() & _lib.DERR_LEN_RANGE
+    assert pkv.device_error() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("block_size", [64, 24, None])  # tcgen05 paged, mma.sync paged, packed k/v
+def test_bad_cu_seqlens_raise_the_range_bit_and_write_nothing(block_size):
+    # a negative start, a negative row count and a sequence longer than max_seqlen_q are
+    # skipped by the prefill kernels' own range checks: nothing is read or written there
+    dev = "cuda"
+    d, hq, hkv = 128, 4, 2
+    q = torch.ones(8, hq, d, dtype=torch.bfloat16, device=dev)
+    kv = torch.ones(8, hkv, d, dtype=torch.bfloat16, device=dev)
+    cases = [([-5, 3], [0, 8], 8), ([0, 4, 2], [0, 4, 6], 8), ([0, 6], [0, 6], 4)]
+    for cu_q, cu_k, max_q in cases:
+        pkv.device_error(reset=True)
+        out = torch.full_like(q, 7.0)
+        kwargs = dict(k=kv, v=kv)
+        if block_size is not None:
+            kc = torch.ones(8, block_size, hkv, d, dtype=torch.bfloat16, device=dev)
+            bt = torch.arange(len(cu_q) - 1, dtype=torch.int32, device=dev)[:, None].contiguous()
+            kwargs = dict(k_cache=kc, v_cache=kc, block_tables=bt)
+        pkv.paged_varlen_prefill_attn(q, torch.tensor(cu_q, dtype=torch.int32, device=dev),
+                                      torch.tensor(cu_k, dtype=torch.int32, device=dev), max_q, 8, 0.1,
+                                      out=out, workspace=False, **kwargs)
+        torch.cuda.synchronize()
+        assert pkv.device_error() & _lib.DERR_LEN_RANGE, (cu_q, cu_k, max_q)
+        if cu_q[1] < 0 or cu_q[0] < 0 or max_q < cu_q[-1] - cu_q[0]:
+            # the single sequence is skipped whole
+            assert torch.all(out == 7.0), (cu_q, cu_k, max_q)
     assert pkv.device_error() == 0
 
 
