@@ -10,9 +10,8 @@ import pagedattention_kv_cache_gb300 as pkv
 from pagedattention_kv_cache_gb300 import metadata as md
 from pagedattention_kv_cache_gb300 import workloads as wl
 from oracle import attention as oa
-from oracle import metadata as om
 
-from _harness import as_np, assert_close, run_decode
+from _harness import as_np, assert_close, decode_layer_full, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -111,34 +110,18 @@ def test_grouped_merge_of_many_parts(group, dtype, lens, splits):
     run_decode(w, num_splits=splits)
 
 
-def test_qwen3_b256_one_layer_full_size_sampled():
+def test_qwen3_b256_one_layer_full_size_every_sequence(oracle_pool):
     # one layer of the 28-layer bench step at full size (batch 256, 4.8 GB of K/V) in the launch the
-    # bench times (automatic split); the longest, the shortest and six random sequences are checked
-    # against the oracle one by one, and their stored rows bit for bit
-    w = wl.qwen3_decode_b256_28l(num_layers=1)
-    t = wl.decode_tensors(w, "cuda")
-    meta = md.decode_metadata(w.block_tables, w.context_lens, w.block_size)
-    gm = md.to_device(meta, "cuda")
-    pkv.kv_store(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], gm["slot_mapping"])
-    ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0)
-    out = pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], gm["block_tables"], gm["context_lens"], w.scale,
-                                workspace=ws)
-    torch.cuda.synchronize()
-    assert pkv.device_error() == 0
-    lens = np.asarray(w.context_lens)
-    rng = np.random.default_rng(7)
-    pick = sorted({int(lens.argmax()), int(lens.argmin())} | set(rng.choice(w.batch, 6, replace=False).tolist()))
-    for b in pick:
-        table = torch.tensor(w.block_tables[b], device="cuda", dtype=torch.long)
-        kb, vb = as_np(t["k_cache"][table]), as_np(t["v_cache"][table])
-        slot = int(meta["slot_mapping"][b])
-        blk, off = divmod(slot, w.block_size)
-        assert torch.equal(t["k_cache"][blk, off], t["k_new"][b]) and torch.equal(t["v_cache"][blk, off], t["v_new"][b])
-        om_ = om.prepare_decode([dict(block_table=list(range(len(w.block_tables[b]))), length=int(lens[b]))],
-                                w.block_size)
-        ref = oa.paged_decode_attention(as_np(t["q"][b:b + 1]), kb, vb, om_["block_tables"], om_["context_lens"],
-                                        w.scale)
-        assert_close(out[b:b + 1], ref, torch.bfloat16, f"batch-256 sequence {b}")
+    # bench times (automatic split): the whole pool against the oracle's store, and all 256
+    # sequences against the oracle's attention
+    decode_layer_full(oracle_pool, wl.qwen3_decode_b256_28l(num_layers=1), 0, "batch-256 layer 0")
+
+
+def test_qwen3_b256_all_28_layers_every_sequence(oracle_pool):
+    # the bench step's other 27 layers, each drawn from its own seed as in the bench
+    w = wl.qwen3_decode_b256_28l()
+    for layer in range(1, w.num_layers):
+        decode_layer_full(oracle_pool, w, layer, f"batch-256 layer {layer}")
 
 
 def test_long_context_split_decode_full_size():

@@ -108,9 +108,10 @@ def _fp8_decode_case(group, splits, q_scale, kv_heads=4, block_size=16, poison=F
     assert_close(out, ref, torch.bfloat16, f"fp8 decode G={group} splits={splits}")
 
 
-def test_fp8_decode_batch256_full_size_sampled():
+def test_fp8_decode_batch256_full_size_every_sequence(oracle_pool):
     # one layer of the bench's FP8 step at full size (batch 256, 2.4 GB of codes) in the launch it
-    # times; the longest, the shortest and six random sequences against the oracle on dequantized blocks
+    # times: the quantizing store of the new tokens bit for bit against the oracle's codec over the
+    # whole pool, then all 256 sequences against the oracle on the dequantized blocks
     w = wl.qwen3_decode_b256_28l(num_layers=1)
     dev = "cuda"
     gen = torch.Generator(device=dev).manual_seed(11)
@@ -118,22 +119,30 @@ def test_fp8_decode_batch256_full_size_sampled():
     kc, vc = [(torch.randn(shape, generator=gen, device=dev) / s).clamp_(-448, 448).to(torch.float8_e4m3fn)
               .view(torch.uint8) for s in (K_SCALE, V_SCALE)]
     q = torch.randn(w.batch, w.num_q_heads, w.head_dim, generator=gen, device=dev).bfloat16()
+    kn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen, device=dev).bfloat16()
+    vn = torch.randn(w.batch, w.num_kv_heads, w.head_dim, generator=gen, device=dev).bfloat16()
     meta = md.decode_metadata(w.block_tables, w.context_lens, w.block_size)
     gm = md.to_device(meta, dev)
+    kc_pre, vc_pre = kc.cpu().numpy(), vc.cpu().numpy()
+    pkv.kv_store_fp8(kn, vn, kc, vc, gm["slot_mapping"], K_SCALE, V_SCALE)
     out = pkv.paged_decode_attn_fp8(q, kc, vc, gm["block_tables"], gm["context_lens"], w.scale, K_SCALE, V_SCALE)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
-    lens = np.asarray(w.context_lens)
-    rng = np.random.default_rng(9)
-    pick = sorted({int(lens.argmax()), int(lens.argmin())} | set(rng.choice(w.batch, 6, replace=False).tolist()))
-    for b in pick:
-        table = torch.tensor(w.block_tables[b], device=dev, dtype=torch.long)
-        kb = of8.dequantize(kc[table].cpu().numpy(), K_SCALE)
-        vb = of8.dequantize(vc[table].cpu().numpy(), V_SCALE)
-        om_ = om.prepare_decode([dict(block_table=list(range(len(w.block_tables[b]))), length=int(lens[b]))],
-                                w.block_size)
-        ref = oa.paged_decode_attention(as_np(q[b:b + 1]), kb, vb, om_["block_tables"], om_["context_lens"], w.scale)
-        assert_close(out[b:b + 1], ref, torch.bfloat16, f"fp8 batch-256 sequence {b}")
+    om_ = om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(w.block_tables, w.context_lens)],
+                            w.block_size)
+    wk, wv = of8.kv_store_fp8(kc_pre, vc_pre, as_np(kn), as_np(vn), om_["slot_mapping"], K_SCALE, V_SCALE)
+    del kc_pre, vc_pre
+    assert np.array_equal(kc.cpu().numpy(), wk) and np.array_equal(vc.cpu().numpy(), wv)
+    del kc, vc
+    views, specs = oracle_pool.shared({"k_codes": (wk.shape, np.uint8), "v_codes": (wv.shape, np.uint8)})
+    views["k_codes"][:] = wk
+    views["v_codes"][:] = wv
+    del views, wk, wv
+    specs.update(q=as_np(q), block_tables=om_["block_tables"], context_lens=om_["context_lens"], scale=w.scale,
+                 k_scale=K_SCALE, v_scale=V_SCALE)
+    ref = oracle_pool.decode_fp8(specs, w.batch)
+    oracle_pool.release()
+    assert_close(out, ref, torch.bfloat16, "fp8 batch-256 layer 0")
 
 
 def test_fp8_argument_errors():

@@ -16,7 +16,7 @@ from pagedattention_kv_cache_gb300 import workloads as wl
 from oracle import attention as oa
 from oracle import metadata as om
 
-from _harness import as_np, assert_close, bits
+from _harness import as_np, assert_close, bits, widen_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -83,38 +83,41 @@ def test_verify_split_part_that_sees_no_key(group):
     run_verify(w, 4, num_splits=9)
 
 
-def test_verify_batch256_q4_full_size_sampled():
-    # the bench's verify case at full size (batch 256, one layer, q_len 4) in the launch it times;
-    # the longest, the shortest and six random sequences are checked against the oracle one by one
+def test_verify_batch256_q4_full_size_every_sequence(oracle_pool):
+    # the bench's verify case at full size (batch 256, one layer, q_len 4) in the launch it times:
+    # the whole pool against the oracle's store, and all 256 sequences' four query rows against the
+    # oracle's varlen prefill definition
     q_len = 4
     w = wl.qwen3_decode_b256_28l(num_layers=1)
     t = wl.verify_tensors(w, q_len, "cuda")
     pm = md.prefill_metadata(w.block_tables, [n - q_len for n in w.context_lens], [q_len] * w.batch, w.block_size)
     dm = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), "cuda")
+    kb_pre, vb_pre = bits(t["k_cache"]), bits(t["v_cache"])
     pkv.kv_store(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], torch.from_numpy(pm["slot_mapping"]).cuda())
     out = pkv.paged_verify_attn(t["q"], t["k_cache"], t["v_cache"], dm["block_tables"], dm["context_lens"], w.scale)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
-    lens = np.asarray(w.context_lens)
-    rng = np.random.default_rng(8)
-    pick = sorted({int(lens.argmax()), int(lens.argmin())} | set(rng.choice(w.batch, 6, replace=False).tolist()))
-    for b in pick:
-        table = torch.tensor(w.block_tables[b], device="cuda", dtype=torch.long)
-        kb, vb = as_np(t["k_cache"][table]), as_np(t["v_cache"][table])
-        n = int(lens[b])
-        local = list(range(len(w.block_tables[b])))
-        om_ = om.prepare_prefill([dict(block_table=local, num_cached_tokens=n - q_len, num_scheduled_tokens=q_len)],
-                                 w.block_size)
-        # the stored rows of this sequence, bit for bit
-        rows = np.arange(n - q_len, n)
-        for i, pos in enumerate(rows):
-            blk, off = divmod(int(pos), w.block_size)
-            assert np.array_equal(bits(t["k_cache"][table[blk], off]), bits(t["k_new"][b * q_len + i]))
-        _, _, hq, d = t["q"].shape
-        ref = oa.paged_prefill_attention(as_np(t["q"][b]).reshape(q_len, hq, d), om_["cu_seqlens_q"],
-                                         om_["cu_seqlens_k"], w.scale, k_cache=kb, v_cache=vb,
-                                         block_tables=om.padded_block_tables([local]))
-        assert_close(out[b], ref, w.dtype, f"verify batch-256 sequence {b}")
+    seqs = [dict(block_table=tb, num_cached_tokens=n - q_len, num_scheduled_tokens=q_len)
+            for tb, n in zip(w.block_tables, w.context_lens)]
+    om_ = om.prepare_prefill(seqs, w.block_size)
+    assert np.array_equal(om_["slot_mapping"], pm["slot_mapping"])
+    kcb, vcb = oa.kv_store(kb_pre, vb_pre, bits(t["k_new"]), bits(t["v_new"]), om_["slot_mapping"])
+    del kb_pre, vb_pre
+    assert np.array_equal(bits(t["k_cache"]), kcb) and np.array_equal(bits(t["v_cache"]), vcb)
+    B, ql, hq, d = t["q"].shape
+    q = as_np(t["q"]).reshape(B * ql, hq, d)
+    del t
+    views, specs = oracle_pool.shared({"k_cache": (kcb.shape, np.float32), "v_cache": (vcb.shape, np.float32),
+                                       "q": (q.shape, np.float32)})
+    widen_bf16_bits(kcb, views["k_cache"])
+    widen_bf16_bits(vcb, views["v_cache"])
+    views["q"][:] = q
+    del views, kcb, vcb
+    specs.update(cu_seqlens_q=om_["cu_seqlens_q"], cu_seqlens_k=om_["cu_seqlens_k"],
+                 block_tables=om.padded_block_tables(w.block_tables), scale=w.scale, causal=True)
+    ref = oracle_pool.prefill(specs, B, B * ql)
+    oracle_pool.release()
+    assert_close(out.reshape(B * ql, hq, d), ref, w.dtype, "verify batch-256 q_len 4")
 
 
 def test_verify_qwen3_batch32_q4():

@@ -367,3 +367,43 @@ def test_copy_blocks_closed_form_and_sharing():
     bt2 = bt.copy()
     bt2[0, 1] = free
     np.testing.assert_array_equal(oa.paged_decode_attention(q, kc2, vc2, bt2, np.array([10]), 0.5), base)
+
+
+def test_parallel_driver_reproduces_the_serial_oracle():
+    # the process-pool driver only fans the loop over sequences out: every row must be the
+    # serial oracle's, bit for bit (decode through shared files, and prefill per sequence)
+    from oracle.parallel import OraclePool
+
+    rng = np.random.default_rng(21)
+    bs, hq, hkv, d = 4, 4, 2, 64
+    lens = [0, 1, 5, 9, 13]
+    nb = sum(-(-n // bs) for n in lens) + 2
+    perm = rng.permutation(nb).tolist()
+    tables, pos = [], 0
+    for n in lens:
+        k = -(-n // bs)
+        tables.append(perm[pos:pos + k])
+        pos += k
+    kc = rng.standard_normal((nb, bs, hkv, d)).astype(np.float32)
+    vc = rng.standard_normal((nb, bs, hkv, d)).astype(np.float32)
+    q = rng.standard_normal((len(lens), hq, d)).astype(np.float32)
+    bt = om.padded_block_tables(tables)
+    cl = np.asarray(lens, dtype=np.int32)
+    want = oa.paged_decode_attention(q, kc, vc, bt, cl, 0.3)
+    with OraclePool(2) as pool:
+        views, specs = pool.shared({"k_cache": (kc.shape, np.float32), "v_cache": (vc.shape, np.float32)})
+        views["k_cache"][:] = kc
+        views["v_cache"][:] = vc
+        specs.update(q=q, block_tables=bt, context_lens=cl, scale=0.3)
+        for chunk in (1, 2):
+            assert np.array_equal(pool.decode(specs, len(lens), chunk=chunk), want)
+        cached, new = [0, 4, 8], [3, 2, 5]
+        tabs = [perm[:1], perm[1:3], perm[3:7]]
+        meta = om.prepare_prefill([dict(block_table=t, num_cached_tokens=c, num_scheduled_tokens=n)
+                                   for t, c, n in zip(tabs, cached, new)], bs)
+        qp = rng.standard_normal((sum(new), hq, d)).astype(np.float32)
+        want_p = oa.paged_prefill_attention(qp, meta["cu_seqlens_q"], meta["cu_seqlens_k"], 0.2, k_cache=kc,
+                                            v_cache=vc, block_tables=meta["block_tables"])
+        specs.update(q=qp, cu_seqlens_q=meta["cu_seqlens_q"], cu_seqlens_k=meta["cu_seqlens_k"],
+                     block_tables=meta["block_tables"], scale=0.2, causal=True)
+        assert np.array_equal(pool.prefill(specs, 3, sum(new)), want_p)
