@@ -17,11 +17,12 @@ Printed (one JSON line, rank 0):
   prefill, prefill_long_history
                the varlen prefill row (16-sequence prefix-cached chunked batch; one sequence
                with a 16k-token history), TFLOP/s against the measured bf16 peak
+  decode_b32   one layer of the batch-32 decode (contexts uniform in [128, 2048]), L2 flushed
   long_context, verify, kv_store, copy_blocks, cuda_graph_decode, fp8_kv
                the other rows: long-context split decode, speculative verify (q_len 4), the
                store alone, copy-on-write block copies, the batch-8 step replayed as a CUDA
                graph, and the step over an E4M3 cache
-  cpu_baseline the CPU oracle timed on a bounded sample of the same workload
+  cpu_baseline the CPU oracle on every host core (all sequences of layer 0), with a one-thread figure
 
 ``--impl reference`` times the CPU oracle itself on bounded samples of the
 same workload (there is no other reference implementation of this path).
@@ -32,7 +33,7 @@ from __future__ import annotations
 import os
 
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")  # the CPU oracle runs on one core; its line says so
+    os.environ.setdefault(_v, "1")  # one thread per oracle process; the parallel oracle uses one process per core
 
 import argparse
 import datetime
@@ -220,6 +221,16 @@ def decode_traffic_record():
 
 
 # ---------------------------------------------------------------- algorithmic work
+
+HBM_NOMINAL_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure the target is stated against
+
+
+def roofline_hbm(gbs: float, hbm_peak: float, **extra) -> dict:
+    """An HBM roofline object: the fraction of the measured copy peak, and of the nominal ~8 TB/s."""
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(gbs / hbm_peak, 4), "frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
+            "nominal_peak": HBM_NOMINAL_GBS, **extra}
+
 
 def decode_alg_bytes(w) -> int:
     elt = torch.finfo(w.dtype).bits // 8
@@ -467,10 +478,9 @@ def bench_fp8(args, device, world):
     result = {"workload": w.name + "-fp8-e4m3", "ms_per_step": round(ms, 4),
               "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
               "decode_tokens_per_s": round(world * w.batch / (ms * 1e-3), 1),
-              "roofline": {"bound": "hbm", "achieved": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                           "unit": "GB/s", "frac": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                           "kernel": "paged_decode_mma_kernel<G=2, e4m3>", "alg_bytes_per_launch": dec_bytes,
-                           "ms_per_launch": round(dec_ms, 5)},
+              "roofline": roofline_hbm(dec_bytes / (dec_ms * 1e-3) / 1e9, hbm_peak,
+                                       kernel="paged_decode_mma_kernel<G=2, e4m3>", alg_bytes_per_launch=dec_bytes,
+                                       ms_per_launch=round(dec_ms, 5)),
               "gpu_launches": 2 * L * args.steps}
     del kc, vc
     torch.cuda.empty_cache()
@@ -511,8 +521,7 @@ def bench_verify(args, device, q_len=4):
     return {"workload": w.name.replace("28layers", "1layer") + f"-verify-q{q_len}", "q_len": q_len,
             "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
             "tokens_per_s": round(w.batch * q_len / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+            "roofline": roofline_hbm(gbs, hbm_peak), "l2": "flushed before each rep"}
 
 
 def bench_long_context(args, device):
@@ -547,8 +556,49 @@ def bench_long_context(args, device):
     torch.cuda.empty_cache()
     return {"workload": w.name, "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
             "kernel": "paged_decode_mma_kernel (G=4), automatic split + fused combine",
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+            "roofline": roofline_hbm(gbs, hbm_peak), "l2": "flushed before each rep"}
+
+
+def bench_decode_b32(args, device):
+    """Qwen3-0.6B-shaped decode of one layer at batch 32, contexts uniform in [128, 2048], block size
+    256, 512-block pool (~143 MB of K/V: L2-sized, so L2 is flushed before each rep)."""
+    import pagedattention_kv_cache_gb300 as pkv
+    from pagedattention_kv_cache_gb300 import metadata as md
+    from pagedattention_kv_cache_gb300 import workloads as wl
+
+    w = wl.qwen3_decode_b32()
+    t = wl.decode_tensors(w, device)
+    meta = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), device)
+    ws = pkv.decode_workspace(w.batch, w.num_q_heads, w.head_dim, 0, device=device)
+    out = torch.empty_like(t["q"])
+    flush = L2Flush(device)
+    times, both = [], []
+    for i in range(args.warmup + max(20, args.steps)):
+        flush_l2(flush)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record()
+        pkv.kv_store(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], meta["slot_mapping"])
+        e1.record()
+        pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], meta["block_tables"], meta["context_lens"],
+                              w.scale, workspace=ws, out=out)
+        e2.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e1.elapsed_time(e2))
+            both.append(e0.elapsed_time(e2))
+    assert pkv.device_error() == 0
+    ms = statistics.median(times)
+    nbytes = decode_alg_bytes(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = measured_peaks()[0]
+    del t
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "batch": w.batch, "context_tokens": sum(w.context_lens), "alg_bytes": nbytes,
+            "ms_median": round(ms, 5), "ms_min": round(min(times), 5), "reps": len(times),
+            "store_and_decode_ms_median": round(statistics.median(both), 5),
+            "value": round(gbs, 1), "unit": UNIT, "decode_tokens_per_s": round(w.batch / (ms * 1e-3), 1),
+            "kernel": "paged_decode_mma_kernel<G=2>, automatic split + fused combine",
+            "roofline": roofline_hbm(gbs, hbm_peak), "l2": "flushed before each rep"}
 
 
 def bench_kv_store(args, device):
@@ -593,8 +643,7 @@ def bench_kv_store(args, device):
         ms = statistics.median(times)
         gbs = nbytes / (ms * 1e-3) / 1e9
         result[name] = {"tokens": n, "alg_bytes": nbytes, "ms_median": round(ms, 5), "value": round(gbs, 1),
-                        "unit": UNIT, "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                                                   "unit": "GB/s", "frac": round(gbs / hbm_peak, 4)}}
+                        "unit": UNIT, "roofline": roofline_hbm(gbs, hbm_peak)}
     assert pkv.device_error() == 0
     result["l2"] = "flushed before each rep"
     result["kernel"] = "kv_store_kernel"
@@ -645,8 +694,7 @@ def bench_cuda_graph(args, device):
             "launches_per_step": 2 * L, "eager_ms_per_step": round(eager_ms, 4),
             "graph_ms_per_step": round(graph_ms, 4), "speedup": round(eager_ms / graph_ms, 3),
             "value": round(gbs, 1), "unit": UNIT, "decode_tokens_per_s": round(w.batch / (graph_ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(gbs / hbm_peak, 4)},
+            "roofline": roofline_hbm(gbs, hbm_peak),
             "l2": "inputs (~4 GB per step) larger than L2, no flush"}
 
 
@@ -684,8 +732,7 @@ def bench_copy_blocks(args, device):
     return {"workload": f"copy-blocks-{pairs}pairs-{L}layers-bs{bs}", "pairs": pairs, "layers": L,
             "alg_bytes": nbytes, "ms_median": round(ms, 4), "value": round(gbs, 1), "unit": UNIT,
             "kernel": "copy_blocks_kernel",
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(gbs / hbm_peak, 4)}, "l2": "flushed before each rep"}
+            "roofline": roofline_hbm(gbs, hbm_peak), "l2": "flushed before each rep"}
 
 
 class L2Flush:
@@ -783,11 +830,78 @@ def oracle_decode_sample(w, state=None, budget_s: float = 12.0, max_seqs: int = 
     return done_bytes, elapsed, nseq
 
 
-def cpu_baseline(w, state=None, budget_s: float = 12.0):
-    nbytes, secs, nseq = oracle_decode_sample(w, state, budget_s)
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"float64 numpy oracle, layer 0 decode attention of {nseq} whole sequences of the same "
-                      f"batch ({nbytes / 1e6:.0f} MB of algorithmic bytes, {secs:.1f} s, one thread)"}
+class OracleAllCores:
+    """The oracle's decode attention over whole sequences of one layer, fanned out over every host
+    core (oracle.parallel: spawned workers, the layer's pool in shared files)."""
+
+    def __init__(self, w, rows, state=None, seed: int = 0):
+        from oracle import metadata as om
+        from oracle.parallel import OraclePool, host_cores
+
+        self.w, self.rows = w, list(rows)
+        self.pool = OraclePool(host_cores())
+        self.cores = self.pool.workers
+        tables = [w.block_tables[b] for b in self.rows]
+        lens = [w.context_lens[b] for b in self.rows]
+        if state is not None:
+            shape = tuple(state.k_cache[0].shape)
+            views, specs = self.pool.shared({"k_cache": (shape, np.float32), "v_cache": (shape, np.float32)})
+            for name, src in (("k_cache", state.k_cache[0]), ("v_cache", state.v_cache[0])):
+                dst = torch.from_numpy(views[name])
+                for i in range(0, shape[0], 256):  # exact bf16 -> float32 widening, a slab at a time
+                    dst[i:i + 256].copy_(src[i:i + 256].float())
+            q = state.q[0][self.rows].float().cpu().numpy()
+            meta = om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(tables, lens)], w.block_size)
+            bt = meta["block_tables"]
+        else:
+            # the sample's blocks drawn on the host (same shapes), numbered in order
+            nblk = [-(-n // w.block_size) for n in lens]
+            shape = (sum(nblk), w.block_size, w.num_kv_heads, w.head_dim)
+            views, specs = self.pool.shared({"k_cache": (shape, np.float32), "v_cache": (shape, np.float32)})
+            gen = torch.Generator().manual_seed(seed)
+            for name in ("k_cache", "v_cache"):
+                dst = torch.from_numpy(views[name])
+                for i in range(0, shape[0], 64):
+                    blk = dst[i:i + 64]
+                    blk.copy_(torch.randn(blk.shape, generator=gen).to(w.dtype).float())
+            q = torch.randn((len(self.rows), w.num_q_heads, w.head_dim), generator=gen).to(w.dtype).float().numpy()
+            starts = np.cumsum([0] + nblk[:-1])
+            local = [list(range(int(s0), int(s0) + k)) for s0, k in zip(starts, nblk)]
+            meta = om.prepare_decode([dict(block_table=t, length=n) for t, n in zip(local, lens)], w.block_size)
+            bt = meta["block_tables"]
+        del views
+        specs.update(q=q, block_tables=bt, context_lens=meta["context_lens"], scale=w.scale)
+        self.specs = specs
+        elt = torch.finfo(w.dtype).bits // 8
+        self.nbytes = sum(n * w.num_kv_heads * w.head_dim * 2 * elt + 2 * w.num_q_heads * w.head_dim * elt
+                          for n in lens)
+        self.pool.decode(self.specs, min(len(self.rows), self.cores))  # workers started and importing done
+
+    def time(self) -> float:
+        t0 = time.perf_counter()
+        self.pool.decode(self.specs, len(self.rows))
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+
+
+def cpu_baseline(w, state=None, budget_s: float = 8.0):
+    """The oracle on every host core (all 256 sequences of layer 0), and on one thread (a bounded
+    sample of whole sequences of the same layer)."""
+    one_bytes, one_secs, one_seqs = oracle_decode_sample(w, state, budget_s)
+    multi = OracleAllCores(w, range(w.batch), state)
+    try:
+        secs = multi.time()
+    finally:
+        multi.close()
+    return {"value": round(multi.nbytes / secs / 1e9, 4), "unit": UNIT, "cores": multi.cores, "kind": "oracle",
+            "sample": f"float64 numpy oracle, layer 0 decode attention of all {w.batch} sequences of the batch "
+                      f"({multi.nbytes / 1e6:.0f} MB of algorithmic bytes) in {secs:.2f} s on {multi.cores} "
+                      f"worker processes, one sequence per task",
+            "one_thread": {"value": round(one_bytes / one_secs / 1e9, 4), "unit": UNIT, "cores": 1,
+                           "sample": f"{one_seqs} whole sequences of layer 0 ({one_bytes / 1e6:.0f} MB) in "
+                                     f"{one_secs:.1f} s"}}
 
 
 def run_reference(args):
@@ -797,22 +911,25 @@ def run_reference(args):
     from pagedattention_kv_cache_gb300 import workloads as wl
 
     w = wl.qwen3_decode_b256_28l()
-    per_step_budget = 4.0
-    for k in range(args.warmup):
-        oracle_decode_sample(w, None, budget_s=0.5, max_seqs=1, seed=100 + k)
-    total_bytes, total_s = 0, 0.0
-    for k in range(args.steps):
-        b, s, _ = oracle_decode_sample(w, None, budget_s=per_step_budget, max_seqs=4, seed=k)
-        total_bytes += b
-        total_s += s
-    value = total_bytes / total_s / 1e9
+    rows = np.random.default_rng(0).permutation(w.batch)[:64].tolist()
+    ref = OracleAllCores(w, rows, None, seed=1)
+    try:
+        for _ in range(args.warmup):
+            ref.time()
+        total_s = sum(ref.time() for _ in range(args.steps))
+    finally:
+        ref.close()
+    value = ref.nbytes * args.steps / total_s / 1e9
+    sample = (f"float64 numpy oracle on {ref.cores} worker processes, decode attention of the same 64 whole "
+              f"sequences of layer 0 per step ({ref.nbytes / 1e6:.0f} MB of algorithmic bytes), blocks drawn on "
+              f"the host")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": "up to 4 whole sequences of layer 0 per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "float64 numpy oracle, decode attention of up to 4 whole sequences per step"},
+        "config": {"workload": w.name, "sample": "64 whole sequences of layer 0 per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": ref.cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -848,10 +965,9 @@ def run_ours(args):
                    w.block_size * w.num_kv_heads * w.head_dim * 2, "l2": "inputs (~139 GB) larger than L2, no flush",
                    "parallelism": f"replicas x{world}"},
         "decode_tokens_per_s": round(world * w.batch / (res["ms_step"] * 1e-3), 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": decode_traffic_record(),
-                     "kernel": "paged_decode_mma_kernel<G=2>", "alg_bytes_per_launch": dec_bytes,
-                     "ms_per_launch": round(dec_ms, 5), "peak_source": f"{peak_src} HBM copy"},
+        "roofline": roofline_hbm(achieved, hbm_peak, traffic=decode_traffic_record(),
+                                 kernel="paged_decode_mma_kernel<G=2>", alg_bytes_per_launch=dec_bytes,
+                                 ms_per_launch=round(dec_ms, 5), peak_source=f"{peak_src} HBM copy"),
         "e2e": e2e,
         "prefill": prefill,
         "gpu_launches": res["launches"],
@@ -863,6 +979,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
     line["fp8_kv"] = bench_fp8(args, device, world)
     line["verify"] = bench_verify(args, device)
+    line["decode_b32"] = bench_decode_b32(args, device)
     line["long_context"] = bench_long_context(args, device)
     line["kv_store"] = bench_kv_store(args, device)
     line["cuda_graph_decode"] = bench_cuda_graph(args, device)
