@@ -308,18 +308,18 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *   block_tables    device, int32 [batch, max_blocks_per_seq] or NULL
  *   total_q, total_k rows of q/out and of the packed k/v (total_k is ignored with block_tables)
  *   causal          1 = causal (bottom-right), 0 = full
- *   workspace       device, 256-byte aligned, or NULL.  When the work items (query
- *                   tiles of 128 / G tokens x KV heads x sequences) are fewer than two per
- *                   SM and the workspace holds at least
+ *   workspace       device, 256-byte aligned, or NULL.  When the work items (pairs of
+ *                   query tiles of 128 / G tokens x KV heads x sequences) are fewer than
+ *                   the SMs and the workspace holds at least
  *                   pkv_paged_varlen_prefill_workspace_bytes(...) bytes, the tensor-core
- *                   kernel runs each query tile with more than 16 key tiles of 64 as up to
+ *                   kernel runs each pair with more than 8 key tiles of 128 as up to
  *                   P parts over consecutive key ranges (P <= 8, enough to fill the GPU)
  *                   and merges them (log-sum-exp, in part order, so results do not depend
  *                   on timing).  Otherwise nothing is split.  It must be zero-filled once
  *                   after allocation; every call leaves it ready for the next one.  Calls
  *                   sharing a workspace must not overlap in time.
  * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.  Block sizes that are a
- * multiple of 64, or a divisor of 64 of at least 8, and the packed path run on
+ * multiple of 128, or a divisor of 128 of at least 8, and the packed path run on
  * the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel (which
  * ignores the workspace).
  */
@@ -337,8 +337,8 @@ int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const
 /*
  * Bytes of the optional workspace of pkv_paged_varlen_prefill_attn for these
  * sizes on the current device: a ticket and a ready count per (sequence, KV
- * head, query tile), each array padded to 256 bytes, then P records of 66,560
- * bytes per item, P as above.  0 when nothing would be split (the items fill
+ * head, query tile; the tiles rounded up to whole pairs), each array padded to
+ * 256 bytes, then P records of 66,560 bytes per query tile, P as above.  0 when nothing would be split (the items fill
  * the GPU, the shape has no tensor-core path, or no device is present).  This
  * sizing rule is the library's own (the pages' flash-attn call has no
  * workspace); it follows the split-decode workspace above.

@@ -34,8 +34,8 @@ struct PrefillArgs {
 };
 
 // Tensor-core (tcgen05 + TMEM + TMA) path; requires head_dim 128, bf16, and
-// for the paged case a block size that is a multiple of 64 or a divisor of
-// 64 of at least 8.
+// for the paged case a block size that is a multiple of 128 or a divisor of
+// 128 of at least 8.
 bool prefill_tc_supported(const PrefillArgs& a);
 int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
 // Workspace bytes that let the tcgen05 path split long items (0: never splits).

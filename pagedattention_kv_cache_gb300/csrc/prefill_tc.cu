@@ -6,27 +6,32 @@
 // history tokens) and, causally, attends keys 0..c + r, read through the
 // block table (or from the packed k/v rows when there is no history).
 //
-// How: a CTA owns one (query tile, sequence, KV head).  The tile's 128 rows
-// are (token, query head of the KV group) pairs, token-major, so one TMA box
-// of q [total_q, Hq, D] covers them and every K/V tile serves all G heads.
-//   warp 0     TMA producer: Q once, then K and V tiles of 64 keys into a
-//              2-stage ring (128-byte swizzled, one box per 64-wide d slab;
-//              paged tiles are gathered block piece by block piece).
-//   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (two S buffers so
-//              the next tile's S overlaps the softmax of this one), then
-//              O += P V with P read from TMEM and V as an MN-major operand.
-//   warps 2-5  softmax, one thread per TMEM lane (= query row): scale, mask,
-//              row max, exp2, bf16 P written back over its S buffer; O is
-//              rescaled in TMEM only when the row max grows by more than 2^8;
-//              final normalisation and store.
-//   warp 6     V guard: zeroes the V rows past the last key in the last tile,
-//              then hands each V tile to the MMA thread.
-// The MMA thread issues and waits alone: a tcgen05.mma issue blocks until the
-// tensor pipe accepts it, so any instruction between two MMA groups is a
-// bubble in the pipe (a blocking try_wait on an already complete barrier costs
-// about 200 cycles there, which is why the waits below try once first).
-// Two CTAs share an SM (256 TMEM columns and ~98 KB of shared memory each),
-// so one CTA's tensor work and loads overlap the other's softmax.
+// How: one CTA per SM owns a pair of query tiles of one (sequence, KV head):
+// tile A and the tile after it, B.  A tile's 128 rows are (token, query head
+// of the KV group) pairs, token-major, so one TMA box of q covers them and
+// every K/V tile serves all G heads of both query tiles.
+//   warp 0     TMA producer: Q of both tiles once, then K and V tiles of 128
+//              keys into 2-stage rings (128-byte swizzled, one box per 64-wide
+//              d slab; paged tiles are gathered block piece by block piece).
+//   warp 1     MMA issuer (one thread).  Per key tile j the tensor pipe runs
+//                 P_A(j) V(j),  Q_A K(j+1)^T,  P_B(j) V(j),  Q_B K(j+1)^T
+//              (each a group of eight M=128, N=128 MMAs), so each tile's
+//              softmax has the other tile's two groups to hide behind.  S and
+//              O of both tiles sit in TMEM (4 x 128 columns); P is written
+//              over S in bf16 and read from TMEM as the A operand of P V.
+//   warps 2-5  softmax of tile A, one thread per TMEM lane (= query row):
+//              scale, mask, row max, exp2, bf16 P; O is rescaled in TMEM only
+//              when the row max grows by more than 2^8; final normalisation
+//              and store.
+//   warps 6-9  the same for tile B.
+//   warp 10    V guard: zeroes the V rows past the last key in the last tile
+//              before the MMA thread may use it.
+// Why this shape (measured on GB300): one issuing thread needs about 45
+// cycles per tcgen05.mma whatever its N, and each barrier wait between MMA
+// groups idles the pipe for ~100 cycles; four groups of N = 128 per key tile
+// keep it busy ~83 % of the time even so, where 32- or 64-key tiles per
+// query tile reached a fifth to a half.  The pair shares every K/V tile,
+// halving the load bytes per flop.
 // Every wait is bounded; on a timeout the CTA records an error, skips the
 // remaining waits and still frees its TMEM.
 #include <algorithm>
@@ -39,55 +44,59 @@ namespace {
 using namespace pkv;
 
 constexpr int kD = 128;
-constexpr int kBM = 128;
-constexpr int kBN = 64;  // keys per tile
-constexpr int kStages = 2;
-constexpr int kThreads = 224;
-constexpr int kGuardWarp = 6;
-constexpr int kCtasPerSm = 2;  // two CTAs share an SM: one's MMA and loads hide the other's softmax
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 2 * kBN;  // S buffers at columns 0 and kBN, O (128 columns) after them
+constexpr int kBM = 128;   // rows per query tile
+constexpr int kBN = 128;   // keys per tile
+constexpr int kStages = 2; // K ring and V ring depth
+constexpr int kSoftmaxWarps = 4;
+constexpr int kGuardWarp = 2 + 2 * kSoftmaxWarps;
+constexpr int kThreads = 32 * (kGuardWarp + 1);
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // S_A at 0, S_B at 128
+constexpr uint32_t kColO = 256;  // O_A at 256, O_B at 384
 constexpr uint32_t kSlabQ = kBM * 128;
 constexpr uint32_t kSlabKV = kBN * 128;
 constexpr uint32_t kTileQ = 2 * kSlabQ;
 constexpr uint32_t kTileKV = 2 * kSlabKV;
-constexpr uint32_t kBarOffset = kTileQ + 2 * kStages * kTileKV;
+constexpr uint32_t kBarOffset = 2 * kTileQ + 2 * kStages * kTileKV;
 constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
-static_assert(kColO + kD <= kTmemCols, "TMEM plan exceeds the allocation");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory plan exceeds an SM");
 constexpr float kRescaleLog2 = 8.0f;
 
-// Key-range split of long work items, used only when the work items do not
-// fill the GPU (small batches with long histories) and a workspace is given.
-// With P parts chosen on the host, an item with more than kSplitMinTiles key
-// tiles runs as up to P CTAs over consecutive ranges of its key tiles.  Every
-// part but the last to finish publishes its unnormalised O and its row maxima
-// and sums (one record per part); the last merges the records and its own TMEM
-// result by the log-sum-exp rule, in part order, and stores the output.
-constexpr int kSplitMinTiles = 16;
+// Key-range split of long work items, used only when the pairs do not fill
+// the GPU (small batches with long histories) and a workspace is given.  With
+// P parts chosen on the host, a pair with more than kSplitMinTiles key tiles
+// runs as up to P CTAs over consecutive ranges of its key tiles.  For each of
+// its two query tiles, every part but the last to finish publishes its
+// unnormalised O and its row maxima and sums (one record per part); the last
+// merges the records and its own TMEM result by the log-sum-exp rule, in part
+// order, and stores the output.
+constexpr int kSplitMinTiles = 8;
 constexpr int kMaxParts = 8;
 constexpr size_t kRecordBytes = static_cast<size_t>(kBM) * kD * 4 + static_cast<size_t>(kBM) * 8;
-constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the second part's wait for the record
+constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the last part's wait for the records
 
-// O_DONE completes once per P.V product; it is waited only one phase behind
-// (lazy rescale).  O_FINAL completes once, after the last P.V: the epilogue and
-// teardown wait on it, because a parity wait on O_DONE could not tell the last
-// phase from one two phases earlier.
-// K and V stages are released separately: a K stage as soon as its Q K^T
-// completes, a V stage when its P V completes, so the producer keeps K two
-// tiles ahead of the tensor pipe.
+// Per query tile X (A = 0, B = 1): S_FULL + X completes when S_X holds the
+// scores of the next key tile, P_FULL + X when its softmax warps have written
+// P over it, O_DONE + X once per P_X V product (waited at most one phase
+// behind, by the lazy rescale).  O_FINAL completes once, after the last MMA:
+// the epilogues and teardown wait on it.  K and V stages are released
+// separately, a K stage once both Q K^T products have read it, a V stage once
+// both P V products have.  V_TAIL: the last V tile, once its rows past the
+// last key are zeroed (only when that tile is partial).
 enum Bar {
   Q_FULL = 0,
   K_FULL = 1,
-  V_FULL = 3,
-  K_EMPTY = 5,
-  V_EMPTY = 7,
-  S_FULL = 9,
-  P_FULL = 11,
-  O_DONE = 13,
-  O_FINAL = 14,
-  V_READY = 15,  // per stage: V loaded and its rows past the last key zeroed
-  NUM_BARS = 17
+  V_FULL = K_FULL + kStages,
+  K_EMPTY = V_FULL + kStages,
+  V_EMPTY = K_EMPTY + kStages,
+  S_FULL = V_EMPTY + kStages,
+  P_FULL = S_FULL + 2,
+  O_DONE = P_FULL + 2,
+  O_FINAL = O_DONE + 2,
+  V_TAIL,
+  NUM_BARS
 };
+static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area too small");
 
 struct TcParams {
   __nv_bfloat16* out;
@@ -107,25 +116,24 @@ struct TcParams {
   int causal;
   int paged;
   int piece_rows;  // rows per K/V TMA box (paged: min(block_size, kBN))
-  int q_tiles;
-  int parts_max;        // P: the most parts a long item runs as (1: no split)
-  int* tickets;         // [items]: finish order of a split item's parts, reset by the last
-  int* ready;           // [items]: records published so far, reset by the last
-  unsigned char* records;  // [items][P][kRecordBytes]: O rows (fp32), then m[kBM], l[kBM]
+  int q_tiles;     // query tiles per sequence, rounded up to a whole number of pairs
+  int parts_max;   // P: the most parts a long pair runs as (1: no split)
+  int* tickets;    // [sequences x KV heads x q_tiles]: finish order of a split tile's parts, reset by the last
+  int* ready;      // [same]: records published so far, reset by the last
+  unsigned char* records;  // [same][P][kRecordBytes]: O rows (fp32), then m[kBM], l[kBM]
 };
 
 }  // namespace
 
 namespace pkv {
 
-// Parts a long item may run as: enough to give every CTA slot (two per SM)
-// work when the items alone do not, at most kMaxParts; 1 when they do.
+// Parts a long pair may run as: enough to give every SM work when the pairs
+// alone do not, at most kMaxParts; 1 when they do.
 int prefill_tc_parts(int batch, int num_kv_heads, int group, int max_seqlen_q, int sms) {
   const long long tq = kBM / group;
-  const long long items = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + tq - 1) / tq);
-  const long long slots = static_cast<long long>(sms) * kCtasPerSm;
-  if (items <= 0 || items >= slots) return 1;
-  return static_cast<int>(std::min<long long>(kMaxParts, (slots + items - 1) / items));
+  const long long pairs = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + 2 * tq - 1) / (2 * tq));
+  if (pairs <= 0 || pairs >= sms) return 1;
+  return static_cast<int>(std::min<long long>(kMaxParts, (sms + pairs - 1) / pairs));
 }
 
 // Workspace of the tcgen05 prefill: tickets and ready counts (256-byte aligned
@@ -139,7 +147,7 @@ size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int ma
   const int parts = prefill_tc_parts(batch, num_kv_heads, group, max_seqlen_q, info.sms);
   if (parts == 1) return 0;
   const long long tq = kBM / group;
-  const long long items = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + tq - 1) / tq);
+  const long long items = static_cast<long long>(batch) * num_kv_heads * 2 * ((max_seqlen_q + 2 * tq - 1) / (2 * tq));
   const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
   return 2 * flags + static_cast<size_t>(items) * parts * kRecordBytes;
 }
@@ -154,6 +162,16 @@ struct Waiter {
   __device__ __forceinline__ void operator()(uint64_t* bar, uint32_t parity) const {
     // one try_wait first: no shared-memory read of the abort flag on the fast path
     if (mbar_try_wait(bar, parity)) return;
+    slow(bar, parity);
+  }
+  // For phases that have usually completed already (loads issued long
+  // before): a test_wait returns at once.
+  __device__ __forceinline__ void ready(uint64_t* bar, uint32_t parity) const {
+    if (mbar_test_wait(bar, parity)) return;
+    if (mbar_try_wait(bar, parity)) return;
+    slow(bar, parity);
+  }
+  __device__ __noinline__ void slow(uint64_t* bar, uint32_t parity) const {
     if (*abort_flag) return;
     if (!mbar_wait(bar, parity)) {
       *abort_flag = 1;
@@ -199,23 +217,23 @@ __device__ __forceinline__ void add_bf16x2(uint64_t& acc, uint32_t w) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   pdl_enter();
   constexpr int TQ = kBM / G;
   // blocks launch in linear order: x runs over (sequence, KV head), y over
-  // query tiles from the last (most keys under the causal mask) to the first,
-  // and, with a workspace, over the two key-range parts of each tile
+  // query-tile pairs from the last (most keys under the causal mask) to the
+  // first, and, with a workspace, over the key-range parts of each pair
   const int seq = blockIdx.x / p.hkv;
   const int g = blockIdx.x % p.hkv;
-  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.y) / p.parts_max;
+  const int pairs = p.q_tiles / 2;
+  const int pt = pairs - 1 - static_cast<int>(blockIdx.y) / p.parts_max;
   const int part = static_cast<int>(blockIdx.y) % p.parts_max;
   const int q_begin = __ldg(p.cu_q + seq);
   const int nq = __ldg(p.cu_q + seq + 1) - q_begin;
   const int k_begin = __ldg(p.cu_k + seq);
   const int nk = __ldg(p.cu_k + seq + 1) - k_begin;
-  const int tok0 = qt * TQ;
   // cu_seqlens must describe rows inside q / out (and the packed k / v), and no
   // sequence may have more rows than max_seqlen_q, which sized the grid: such a
   // sequence is skipped whole and raises the range bit
@@ -225,31 +243,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (threadIdx.x == 0) raise_error(p.err, PKV_DERR_LEN_RANGE);
     return;
   }
+  const int tok0 = pt * 2 * TQ;  // first token of tile A; tile B starts TQ later
   if (tok0 >= nq) return;
   const int cached = nk - nq;
-  const int tok_last = min(nq, tok0 + TQ) - 1;
-  const int keys_needed = p.causal ? cached + tok_last + 1 : nk;
-  const int n_all = (keys_needed + kBN - 1) / kBN;
+  // key tiles each query tile needs (0: the tile has no rows)
+  int n_need[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int t0 = tok0 + x * TQ;
+    const int keys = t0 >= nq ? 0 : (p.causal ? cached + min(nq, t0 + TQ) : nk);
+    n_need[x] = (keys + kBN - 1) / kBN;
+  }
+  const int n_all = max(n_need[0], n_need[1]);
   // this CTA's key tiles: j0 .. j0 + n_tiles - 1 (all of them, or one of up to P
-  // consecutive ranges)
+  // consecutive ranges); tile X takes the first n_x of them
   const int parts = n_all > kSplitMinTiles ? min(p.parts_max, (n_all + kSplitMinTiles - 1) / kSplitMinTiles) : 1;
   if (part >= parts) return;
   const int j0 = part * n_all / parts;
   const int n_tiles = (part + 1) * n_all / parts - j0;
+  const int n_a = max(0, min(n_tiles, n_need[0] - j0));
+  const int n_b = max(0, min(n_tiles, n_need[1] - j0));
+  // the last tile holds keys past nk: its V rows there are zeroed first
+  const bool v_tail = (j0 + n_tiles) * kBN > nk;
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  unsigned char* sq = smem;
-  unsigned char* sk = smem + kTileQ;
+  unsigned char* sq = smem;  // Q_A, then Q_B
+  unsigned char* sk = sq + 2 * kTileQ;
   unsigned char* sv = sk + kStages * kTileKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* s_ticket = abort_flag + 1;  // a split item's ticket, broadcast to the softmax warps
+  volatile int* s_ticket = abort_flag + 1;  // split tiles' tickets, one per query tile
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
   const int lane = tid % 32;
+  const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
+  if (tid == 32 && p.paged && n_tiles > 0) {
+    // warm the first block-table entries the producer needs, while the CTA sets up
+    uint32_t warm;
+    const int blk0 = j0 * kBN / p.block_size;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(warm) : "l"(table + blk0) : "memory");
+    if (n_tiles > 1) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(warm) : "l"(table + (j0 + 1) * kBN / p.block_size) : "memory");
+  }
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -259,14 +296,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&bars[V_FULL + s], 1);
       mbar_init(&bars[K_EMPTY + s], 1);
       mbar_init(&bars[V_EMPTY + s], 1);
-      mbar_init(&bars[V_READY + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[S_FULL + b], 1);
-      mbar_init(&bars[P_FULL + b], 4);  // one arrival per softmax warp
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[S_FULL + x], 1);
+      mbar_init(&bars[P_FULL + x], kSoftmaxWarps);
+      mbar_init(&bars[O_DONE + x], 1);
     }
-    mbar_init(&bars[O_DONE], 1);
     mbar_init(&bars[O_FINAL], 1);
+    mbar_init(&bars[V_TAIL], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -286,12 +323,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tc::prefetch_tensormap(&tm_q);
       tc::prefetch_tensormap(&tm_k);
       tc::prefetch_tensormap(&tm_v);
-      mbar_expect_tx(&bars[Q_FULL], kTileQ);
-      tc::tma_load_3d(sq, &tm_q, 0, g * G, q_begin + tok0, &bars[Q_FULL]);
-      tc::tma_load_3d(sq + kSlabQ, &tm_q, 64, g * G, q_begin + tok0, &bars[Q_FULL]);
+      const int nx = n_b > 0 ? 2 : 1;
+      mbar_expect_tx(&bars[Q_FULL], nx * kTileQ);
+      for (int x = 0; x < nx; ++x) {
+        tc::tma_load_3d(sq + x * kTileQ, &tm_q, 0, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
+        tc::tma_load_3d(sq + x * kTileQ + kSlabQ, &tm_q, 64, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
+      }
       mbar_arrive(&bars[Q_FULL]);
-      const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-      // Loads one tile's K (is_v = false) or V into stage j % kStages, after the
+      // Loads tile j's K (is_v = false) or V into stage j % kStages, after the
       // stage's previous occupant (tile j - kStages) was released.
       auto load_tile = [&](int j, bool is_v) {
         const int st = j % kStages;
@@ -325,11 +364,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         mbar_arrive(full);
       };
-      // issue order K0, K1, V0, K2, V1, K3, ...: K runs two tiles ahead
-      for (int j = 0; j < kStages && j < n_tiles; ++j) load_tile(j, false);
+      // K(j) once the K stage is free (both Q K^T of tile j - 2 read it), V(j)
+      // once the V stage is
       for (int j = 0; j < n_tiles; ++j) {
+        load_tile(j, false);
         load_tile(j, true);
-        if (j + kStages < n_tiles) load_tile(j + kStages, false);
       }
     }
   } else if (warp == 1) {
@@ -342,36 +381,61 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint64_t q_desc = tc::smem_desc(smem_u32(sq), 16, 1024);
       const uint64_t k_desc = tc::smem_desc(smem_u32(sk), 16, 1024);
       const uint64_t v_desc = tc::smem_desc(smem_u32(sv), kSlabKV, 1024);
-      wait(&bars[Q_FULL], 0);
-      // S(j) = Q K(j)^T into S buffer j & 1
-      auto issue_qk = [&](int j) {
+      const int n_x[2] = {n_a, n_b};
+      // S_X = Q_X K(j)^T (S_X held P_X(j - 1), read by P_X(j - 1) V issued
+      // before: the tensor pipe runs one thread's MMAs in order)
+      auto issue_qk = [&](int x, int j) {
         const int st = j % kStages;
-        wait(&bars[K_FULL + st], (j / kStages) & 1);
-        tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kSlabQ + (kk & 3) * 32;
+          const uint32_t a_off = x * kTileQ + (kk >> 2) * kSlabQ + (kk & 3) * 32;
           const uint32_t b_off = st * kTileKV + (kk >> 2) * kSlabKV + (kk & 3) * 32;
-          tc::mma_ss(tmem + (j & 1) * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
+          tc::mma_ss(tmem + kColS + x * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
         }
-        tc::commit(&bars[S_FULL + (j & 1)]);
-        tc::commit(&bars[K_EMPTY + st]);
+        tc::commit(&bars[S_FULL + x]);
       };
-      issue_qk(0);
-      for (int j = 0; j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) issue_qk(j + 1);  // its S buffer held P(j - 1), consumed already
+      // O_X += P_X(j) V(j)
+      auto issue_pv = [&](int x, int j) {
         const int st = j % kStages;
-        wait(&bars[V_READY + st], (j / kStages) & 1);
-        wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1);
+        wait(&bars[P_FULL + x], j & 1);
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t b_off = st * kTileKV + kk * 16 * 128;
-          tc::mma_ts(tmem + kColO, tmem + (j & 1) * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
+          tc::mma_ts(tmem + kColO + x * kD, tmem + kColS + x * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
         }
+        tc::commit(&bars[O_DONE + x]);
+      };
+      wait(&bars[Q_FULL], 0);
+      if (n_tiles > 0) {
+        wait.ready(&bars[K_FULL], 0);
+        tc::fence_after_sync();
+        for (int x = 0; x < 2; ++x)
+          if (n_x[x] > 0) issue_qk(x, 0);
+        tc::commit(&bars[K_EMPTY]);
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kStages;
+        if (v_tail && j == n_tiles - 1)
+          wait(&bars[V_TAIL], 0);
+        else
+          wait.ready(&bars[V_FULL + st], (j / kStages) & 1);
+        const bool next = j + 1 < n_tiles;
+        bool k_next = false;  // K(j + 1) seen loaded
+        for (int x = 0; x < 2; ++x) {
+          if (j < n_x[x]) issue_pv(x, j);
+          if (j + 1 < n_x[x]) {
+            if (!k_next) {
+              wait.ready(&bars[K_FULL + (j + 1) % kStages], ((j + 1) / kStages) & 1);
+              tc::fence_after_sync();
+              k_next = true;
+            }
+            issue_qk(x, j + 1);
+          }
+        }
         tc::commit(&bars[V_EMPTY + st]);
-        tc::commit(&bars[O_DONE]);
+        if (next) tc::commit(&bars[K_EMPTY + (j + 1) % kStages]);
       }
       tc::commit(&bars[O_FINAL]);
       // no MMA may be in flight when TMEM is freed
@@ -379,61 +443,67 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == kGuardWarp) {
     // ------------------------------------------------------------ V guard
-    // Follows every V_FULL phase; in the last tile the V rows past the last key
-    // hold whatever their block had there (or were not loaded): zero them so
-    // 0 * stale never reaches O, then release the tile to the MMA thread.
-    for (int j = 0; j < n_tiles; ++j) {
+    // In the last tile the V rows past nk hold whatever their block had there
+    // (or were not loaded): zero them so 0 * stale never reaches O.
+    if (v_tail) {
+      const int j = n_tiles - 1;
       const int st = j % kStages;
-      wait(&bars[V_FULL + st], (j / kStages) & 1);
-      const int key0 = (j0 + j) * kBN;
-      if (key0 + kBN > nk) {
-        unsigned char* vt = sv + st * kTileKV;
-        const int first = nk - key0;
-        for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
-          const int rr = first + idx / 16;
-          const int ch = idx % 16;
-          *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // follow the stage's phases in order up to the last tile's: a parity wait
+      // for a phase two or more ahead would return at once
+      for (int t = st; t <= j; t += kStages) wait(&bars[V_FULL + st], (t / kStages) & 1);
+      unsigned char* vt = sv + st * kTileKV;
+      const int first = nk - (j0 + j) * kBN;
+      for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
+        const int rr = first + idx / 16;
+        const int ch = idx % 16;
+        *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[V_READY + st]);
+      if (lane == 0) mbar_arrive(&bars[V_TAIL]);
     }
   } else {
-    // ------------------------------------------------------------ softmax + epilogue
+    // ------------------------------------------------------------ softmax + epilogue of tile X
+    const int x = (warp - 2) / kSoftmaxWarps;
+    const int n_x = x == 0 ? n_a : n_b;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int tok = tok0 + row / G;
+    const int tok_first = tok0 + x * TQ;  // first token of this query tile
+    const int tok = tok_first + row / G;
     const int head = row % G;
     const int pos = cached + tok;  // absolute position of this query row
     const bool row_valid = tok < nq;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t s_addr = lane_addr + kColS + x * kBN;
+    const uint32_t o_addr = lane_addr + kColO + x * kD;
     const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
     float m_run = -INFINITY;
     float l_run = 0.f;
-    uint32_t r[kBN];
+    uint32_t r[32];
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
+    for (int j = 0; j < n_x; ++j) {
       const int key0 = (j0 + j) * kBN;
-      wait(&bars[S_FULL + b], (j >> 1) & 1);
+      wait(&bars[S_FULL + x], j & 1);
       tc::fence_after_sync();
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(lane_addr + b * kBN + c * 32, r + c * 32);
-      tc::tmem_wait_ld();
-      if (key0 + kBN - 1 > (p.causal ? cached + tok0 : nk - 1)) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (key0 + c > lim) r[c] = __float_as_uint(-INFINITY);
-      }
-      // row maximum of the raw scores (the scale, > 0, is applied after), as
-      // four independent chains of three-input maxima
+      const bool masked = key0 + kBN - 1 > (p.causal ? cached + tok_first : nk - 1);
+      // pass 1: row maximum of the raw scores (the scale, > 0, is applied
+      // after), 32 columns at a time, as four chains of three-input maxima
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
+      for (int c = 0; c < kBN / 32; ++c) {
+        tc::tmem_ld32(s_addr + c * 32, r);
+        tc::tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          mx[u] = max3(mx[u], __uint_as_float(r[c + 2 * u]), __uint_as_float(r[c + 2 * u + 1]));
+          for (int e = 0; e < 32; ++e)
+            if (key0 + c * 32 + e > lim) r[e] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx[u] = max3(mx[u], __uint_as_float(r[e + 2 * u]), __uint_as_float(r[e + 2 * u + 1]));
+        }
       }
       const float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       const float m_new = fmaxf(m_run, mt * p.scale_log2);
@@ -445,15 +515,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m_run = fmaxf(m_run, m_new);
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      // P = exp2(scale * s - m) rounded to bf16, packed two per column over the
-      // S buffer; the row sum adds the same rounded values (four accumulators
-      // of two lanes, so the adds do not form one long chain)
+      // pass 2: P = exp2(scale * s - m) rounded to bf16, packed two per column
+      // over the first half of S (chunk c's 16 columns overwrite scores that
+      // earlier chunks already consumed); the row sum adds the same rounded
+      // values (four accumulators of two lanes, so the adds do not form one
+      // long chain)
       uint64_t l_pair[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const uint32_t w = exp2_pair_bf16(r[2 * c], r[2 * c + 1], p.scale_log2, -m_use);
-        add_bf16x2(l_pair[c % 4], w);
-        r[c] = w;
+      for (int c = 0; c < kBN / 32; ++c) {
+        tc::tmem_ld32(s_addr + c * 32, r);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (key0 + c * 32 + e > lim) r[e] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t w = exp2_pair_bf16(r[2 * e], r[2 * e + 1], p.scale_log2, -m_use);
+          add_bf16x2(l_pair[e % 4], w);
+          r[e] = w;
+        }
+        tc::tmem_st16(s_addr + c * 16, r);
       }
       float l_tile = 0.f;
 #pragma unroll
@@ -461,67 +544,92 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         l_tile += __uint_as_float(static_cast<uint32_t>(l_pair[u])) +
                   __uint_as_float(static_cast<uint32_t>(l_pair[u] >> 32));
       l_run = l_run * factor + l_tile;
-#pragma unroll
-      for (int c = 0; c < kBN / 64; ++c) tc::tmem_st32(lane_addr + b * kBN + c * 32, r + c * 32);
       if (rescale && j > 0) {
-        // O holds the products up to tile j-1: wait for P.V(j-1) (one phase
-        // back at most, see above), then bring O to the new maximum
-        wait(&bars[O_DONE], (j - 1) & 1);
+        // O_X holds the products up to tile j-1 (complete: S_X(j) was written
+        // after P_X(j-1) V); bring it to the new maximum
+        wait(&bars[O_DONE + x], (j - 1) & 1);
         tc::fence_after_sync();
         uint32_t o[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          tc::tmem_ld32(lane_addr + kColO + c * 32, o);
+          tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tc::tmem_st32(lane_addr + kColO + c * 32, o);
+          tc::tmem_st32(o_addr + c * 32, o);
         }
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[P_FULL + b]);
+      if (lane == 0) mbar_arrive(&bars[P_FULL + x]);
     }
 
     wait(&bars[O_FINAL], 0);
     tc::fence_after_sync();
     __nv_bfloat16* dst =
         p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + head) * kD;
+    // this thread's 128 outputs, 32 at a time: TMEM O (zero when the tile saw no key in this part)
+    auto load_o = [&](int c, uint32_t* o) {
+      if (n_x > 0) {
+        tc::tmem_ld32(o_addr + c * 32, o);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+    };
     if (parts == 1) {
+      // normalised bf16 rows staged in this tile's Q buffer (free: every MMA has
+      // completed), 16-byte chunk c of row r at chunk position c ^ (r & 15) so
+      // the eight rows of a quarter-warp hit distinct banks; then copied out
+      // two rows (512 contiguous bytes when G > 1) per warp instruction
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      unsigned char* stage = sq + x * kTileQ;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(lane_addr + kColO + c * 32, o);
-        tc::tmem_wait_ld();
-        if (row_valid) {
+        load_o(c, o);
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float f[8];
+        for (int e = 0; e < 32; e += 8) {
+          float f[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
-            reinterpret_cast<uint4*>(dst + c * 32 + e)[0] = Chunk<__nv_bfloat16>::pack(f);
-          }
+          for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
+          const int chunk = (c * 32 + e) / 8;
+          *reinterpret_cast<uint4*>(stage + row * 256 + ((chunk ^ (row & 15)) << 4)) = Chunk<__nv_bfloat16>::pack(f);
         }
       }
-    } else {
-      // Split item: every part but the last to finish publishes O (unnormalised),
+      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+      const int t = row;  // 0..127 within the tile's softmax warps
+#pragma unroll 4
+      for (int k = 0; k < kBM / 8; ++k) {
+        const int rr = k * 8 + t / 16;
+        const int chunk = t % 16;
+        const int tk = tok_first + rr / G;
+        if (tk < nq) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + ((chunk ^ (rr & 15)) << 4));
+          __nv_bfloat16* o_row = p.out + (static_cast<size_t>(q_begin + tk) * p.hq + g * G + rr % G) * kD;
+          reinterpret_cast<uint4*>(o_row)[chunk] = v;
+        }
+      }
+    } else if (tok_first < nq) {
+      // Split tile: every part but the last to finish publishes O (unnormalised),
       // m and l of each row; the last waits for those records and merges.
+      const int qt = 2 * pt + x;
       const long long item = (static_cast<long long>(seq) * p.hkv + g) * p.q_tiles + qt;
+      const int leader = 64 + x * 32 * kSoftmaxWarps;  // first thread of this tile's softmax warps
       auto record = [&](int q) {
         return reinterpret_cast<float*>(p.records + (static_cast<size_t>(item) * p.parts_max + q) * kRecordBytes);
       };
-      named_barrier_sync(1, 128);
-      if (threadIdx.x == 64) *s_ticket = atomicAdd(p.tickets + item, 1);
-      named_barrier_sync(1, 128);
-      if (*s_ticket < parts - 1) {
+      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+      if (threadIdx.x == leader) s_ticket[x] = atomicAdd(p.tickets + item, 1);
+      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+      if (s_ticket[x] < parts - 1) {
         float* rec = record(part);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(lane_addr + kColO + c * 32, o);
-          tc::tmem_wait_ld();
+          load_o(c, o);
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             reinterpret_cast<uint4*>(rec + row * kD + c * 32 + e)[0] = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
@@ -529,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         rec[kBM * kD + row] = m_run;
         rec[kBM * kD + kBM + row] = l_run;
         __threadfence();
-        named_barrier_sync(1, 128);
-        if (threadIdx.x == 64) atomicAdd(p.ready + item, 1);
+        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+        if (threadIdx.x == leader) atomicAdd(p.ready + item, 1);
       } else {
-        if (threadIdx.x == 64) {
+        if (threadIdx.x == leader) {
           // the other parts hold their tickets, so they are resident and publish
           // soon; the wait is still bounded
           const uint64_t t0 = globaltimer_ns();
@@ -548,11 +656,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             __nanosleep(100);
           }
           if (!ok) raise_error(p.err, PKV_DERR_WAIT_TIMEOUT);
-          *s_ticket = ok ? 1 : -1;
+          s_ticket[x] = ok ? 1 : -1;
         }
-        named_barrier_sync(1, 128);
+        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
         __threadfence();
-        if (*s_ticket == 1) {
+        if (s_ticket[x] == 1) {
           // log-sum-exp merge over the parts that saw a key of this row, in part
           // order, so the result does not depend on the order they finished in
           float mq[kMaxParts], lq[kMaxParts];
@@ -577,8 +685,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tc::tmem_ld32(lane_addr + kColO + c * 32, o);
-            tc::tmem_wait_ld();
+            load_o(c, o);
             if (row_valid) {
 #pragma unroll
               for (int e = 0; e < 32; e += 8) {
@@ -586,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int q = 0; q < kMaxParts; ++q) {
                   if (q >= parts) break;
+                  if (mq[q] == 0.f) continue;  // saw no key of this row: weight 0, record not read
                   float v8[8];
                   if (q == part) {
 #pragma unroll
@@ -607,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
           }
         }
-        named_barrier_sync(1, 128);
-        if (threadIdx.x == 64) {  // leave the item's slots ready for the next call
+        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+        if (threadIdx.x == leader) {  // leave the tile's slots ready for the next call
           p.tickets[item] = 0;
           p.ready[item] = 0;
         }
@@ -654,7 +762,8 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.paged = paged ? 1 : 0;
   p.piece_rows = piece;
-  p.q_tiles = (a.max_seqlen_q + TQ - 1) / TQ;
+  const int pairs = (a.max_seqlen_q + 2 * TQ - 1) / (2 * TQ);
+  p.q_tiles = 2 * pairs;
   p.parts_max = 1;
   DeviceInfo info;
   if (device_info(&info) != PKV_OK) return PKV_ECUDA;
@@ -672,7 +781,7 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
       cudaSuccess)
     return PKV_ECUDA;
-  dim3 grid(a.batch * a.hkv, p.q_tiles * p.parts_max);
+  dim3 grid(a.batch * a.hkv, pairs * p.parts_max);
   return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, tm_q, tm_k, tm_v, p) == cudaSuccess ? PKV_OK
                                                                                                   : PKV_ECUDA;
 }

@@ -60,18 +60,20 @@ def test_prefill_workspace_is_zero_when_nothing_splits():
 
 @pytest.mark.gpu
 def test_prefill_workspace_size_rule():
-    # P = ceil(2 * SMs / items) parts (at most 8) when the items are fewer than two per SM; then one int
-    # ticket and one int ready count per (sequence, KV head, query tile of 128 / G tokens), each array
-    # padded to 256 bytes, and P records of 128 rows x (128 fp32 + m + l) per item
+    # work items are pairs of query tiles of 128 / G tokens, one CTA per SM: P = ceil(SMs / pairs) parts
+    # (at most 8) when the pairs are fewer than the SMs; then one int ticket and one int ready count per
+    # (sequence, KV head, query tile), each array padded to 256 bytes, and P records of
+    # 128 rows x (128 fp32 + m + l) per query tile
     lib = _lib.load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
     def expect(batch, hq, hkv, max_q):
         tq = 128 // (hq // hkv)
-        items = batch * hkv * (-(-max_q // tq))
-        if items >= 2 * sms:
+        pairs = batch * hkv * (-(-max_q // (2 * tq)))
+        if pairs >= sms:
             return 0
-        parts = min(8, -(-2 * sms // items))
+        parts = min(8, -(-sms // pairs))
+        items = 2 * pairs
         flags = -(-items * 4 // 256) * 256
         return 2 * flags + items * parts * (128 * 128 * 4 + 128 * 8)
 

@@ -22,7 +22,7 @@ def test_qwen3_prefill_prefix_chunk_poisoned():
 
 
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-@pytest.mark.parametrize("block_size", [4, 8, 16, 24, 64, 256])
+@pytest.mark.parametrize("block_size", [4, 8, 16, 24, 32, 48, 64, 96, 256])
 def test_prefill_groups_and_block_sizes(group, block_size):
     w = wl.random_prefill(group * 10 + block_size, batch=5, max_new=150, min_new=1, max_cached_blocks=3,
                           block_size=block_size, num_q_heads=2 * group, num_kv_heads=2, head_dim=128)
@@ -109,8 +109,8 @@ def test_prefill_many_short_sequences_repeated():
 
 
 def _long_history(seed: int, group: int = 2, block_size: int = 256) -> wl.PrefillWorkload:
-    # histories of up to 12 blocks of 256: the last query tiles need ~50 key tiles of 64,
-    # far past the 16 above which a tile runs as two parts
+    # histories of up to 12 blocks of 256: the last query tiles need ~25 key tiles of 128,
+    # far past the 8 above which a tile runs as several parts
     return wl.random_prefill(seed, batch=3, max_new=300, min_new=40, max_cached_blocks=12, block_size=block_size,
                              num_q_heads=8 * group, num_kv_heads=8, head_dim=128)
 
@@ -145,7 +145,7 @@ def test_split_workspace_reused_and_left_zeroed():
 
 def test_single_long_history_runs_as_eight_parts():
     # one sequence, a 16k-token history and 200 new tokens: 32 work items for a GPU with ~300 CTA slots,
-    # so each query tile (259 key tiles) runs as eight parts
+    # so each query tile (130 key tiles of 128) runs as eight parts
     w = wl.random_prefill(37, batch=1, max_new=200, min_new=200, max_cached_blocks=64, block_size=256,
                           num_q_heads=16, num_kv_heads=8, head_dim=128)
     w.num_cached[0] = 64 * 256
