@@ -309,11 +309,11 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *   total_q, total_k rows of q/out and of the packed k/v (total_k is ignored with block_tables)
  *   causal          1 = causal (bottom-right), 0 = full
  *   workspace       device, 256-byte aligned, or NULL.  When the work items (pairs of
- *                   query tiles of 128 / G tokens x KV heads x sequences) are fewer than
- *                   the SMs and the workspace holds at least
+ *                   query tiles of 128 / G tokens x KV heads x sequences) fill at most
+ *                   half the SMs and the workspace holds at least
  *                   pkv_paged_varlen_prefill_workspace_bytes(...) bytes, the tensor-core
  *                   kernel runs each pair with more than 8 key tiles of 128 as up to
- *                   P parts over consecutive key ranges (P <= 8, enough to fill the GPU)
+ *                   P = min(8, SMs / pairs) parts over consecutive key ranges
  *                   and merges them (log-sum-exp, in part order, so results do not depend
  *                   on timing).  Otherwise nothing is split.  It must be zero-filled once
  *                   after allocation; every call leaves it ready for the next one.  Calls

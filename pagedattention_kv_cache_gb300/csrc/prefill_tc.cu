@@ -10,22 +10,23 @@
 // tile A and the tile after it, B.  A tile's 128 rows are (token, query head
 // of the KV group) pairs, token-major, so one TMA box of q covers them and
 // every K/V tile serves all G heads of both query tiles.
-//   warp 0     TMA producer: Q of both tiles once, then K and V tiles of 128
-//              keys into 2-stage rings (128-byte swizzled, one box per 64-wide
-//              d slab; paged tiles are gathered block piece by block piece).
+//   warp 0     TMA producer (one thread): Q of both tiles once, then K and V
+//              tiles of 128 keys into 2-stage rings (128-byte swizzled, one
+//              box per 64-wide d slab; paged tiles are gathered block piece by
+//              block piece).  Then the whole warp zeroes the V rows past the
+//              last key in the last tile before the MMA thread may use it.
 //   warp 1     MMA issuer (one thread).  Per key tile j the tensor pipe runs
 //                 P_A(j) V(j),  Q_A K(j+1)^T,  P_B(j) V(j),  Q_B K(j+1)^T
 //              (each a group of eight M=128, N=128 MMAs), so each tile's
 //              softmax has the other tile's two groups to hide behind.  S and
 //              O of both tiles sit in TMEM (4 x 128 columns); P is written
 //              over S in bf16 and read from TMEM as the A operand of P V.
-//   warps 2-5  softmax of tile A, one thread per TMEM lane (= query row):
-//              scale, mask, row max, exp2, bf16 P; O is rescaled in TMEM only
-//              when the row max grows by more than 2^8; final normalisation
-//              and store.
-//   warps 6-9  the same for tile B.
-//   warp 10    V guard: zeroes the V rows past the last key in the last tile
-//              before the MMA thread may use it.
+//   warps 2-9  softmax of tile A, two threads per TMEM lane (= query row),
+//              one per half of the key tile: scale, mask, row max (the halves
+//              exchange theirs through shared memory), exp2, bf16 P; O is
+//              rescaled in TMEM only when the row max grows by more than 2^8;
+//              final normalisation and store (each half 64 of the 128 columns).
+//   warps 10-17  the same for tile B.
 // Why this shape (measured on GB300): one issuing thread needs about 45
 // cycles per tcgen05.mma whatever its N, and each barrier wait between MMA
 // groups idles the pipe for ~100 cycles; four groups of N = 128 per key tile
@@ -47,9 +48,8 @@ constexpr int kD = 128;
 constexpr int kBM = 128;   // rows per query tile
 constexpr int kBN = 128;   // keys per tile
 constexpr int kStages = 2; // K ring and V ring depth
-constexpr int kSoftmaxWarps = 4;
-constexpr int kGuardWarp = 2 + 2 * kSoftmaxWarps;
-constexpr int kThreads = 32 * (kGuardWarp + 1);
+constexpr int kSoftmaxWarps = 8;  // per query tile: two threads per row, one per half of the key tile
+constexpr int kThreads = 32 * (2 + 2 * kSoftmaxWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_A at 0, S_B at 128
 constexpr uint32_t kColO = 256;  // O_A at 256, O_B at 384
@@ -57,7 +57,9 @@ constexpr uint32_t kSlabQ = kBM * 128;
 constexpr uint32_t kSlabKV = kBN * 128;
 constexpr uint32_t kTileQ = 2 * kSlabQ;
 constexpr uint32_t kTileKV = 2 * kSlabKV;
-constexpr uint32_t kBarOffset = 2 * kTileQ + 2 * kStages * kTileKV;
+constexpr uint32_t kRedOffset = 2 * kTileQ + 2 * kStages * kTileKV;  // row maxima / sums exchanged by the halves
+constexpr uint32_t kRedBytes = 2 * 2 * 2 * kBM * 4;                  // [tile parity][query tile][half][row]
+constexpr uint32_t kBarOffset = kRedOffset + kRedBytes;
 constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory plan exceeds an SM");
 constexpr float kRescaleLog2 = 8.0f;
@@ -78,8 +80,8 @@ constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the last part's wa
 // Per query tile X (A = 0, B = 1): S_FULL + X completes when S_X holds the
 // scores of the next key tile, P_FULL + X when its softmax warps have written
 // P over it, O_DONE + X once per P_X V product (waited at most one phase
-// behind, by the lazy rescale).  O_FINAL completes once, after the last MMA:
-// the epilogues and teardown wait on it.  K and V stages are released
+// behind, by the lazy rescale).  O_FINAL + X completes once, after the last
+// P_X V: tile X's epilogue waits on it (A's can start while B still runs).  K and V stages are released
 // separately, a K stage once both Q K^T products have read it, a V stage once
 // both P V products have.  V_TAIL: the last V tile, once its rows past the
 // last key are zeroed (only when that tile is partial).
@@ -92,8 +94,8 @@ enum Bar {
   S_FULL = V_EMPTY + kStages,
   P_FULL = S_FULL + 2,
   O_DONE = P_FULL + 2,
-  O_FINAL = O_DONE + 2,
-  V_TAIL,
+  O_FINAL = O_DONE + 2,  // per query tile
+  V_TAIL = O_FINAL + 2,
   NUM_BARS
 };
 static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area too small");
@@ -127,13 +129,14 @@ struct TcParams {
 
 namespace pkv {
 
-// Parts a long pair may run as: enough to give every SM work when the pairs
-// alone do not, at most kMaxParts; 1 when they do.
+// Parts a long pair may run as when the pairs alone leave SMs idle: as many
+// as fit in one wave of one CTA per SM (at most kMaxParts), so the split
+// never adds a second, mostly empty wave; 1 when the pairs fill the GPU.
 int prefill_tc_parts(int batch, int num_kv_heads, int group, int max_seqlen_q, int sms) {
   const long long tq = kBM / group;
   const long long pairs = static_cast<long long>(batch) * num_kv_heads * ((max_seqlen_q + 2 * tq - 1) / (2 * tq));
-  if (pairs <= 0 || pairs >= sms) return 1;
-  return static_cast<int>(std::min<long long>(kMaxParts, (sms + pairs - 1) / pairs));
+  if (pairs <= 0 || 2 * pairs > sms) return 1;
+  return static_cast<int>(std::min<long long>(kMaxParts, sms / pairs));
 }
 
 // Workspace of the tcgen05 prefill: tickets and ready counts (256-byte aligned
@@ -271,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sq = smem;  // Q_A, then Q_B
   unsigned char* sk = sq + 2 * kTileQ;
   unsigned char* sv = sk + kStages * kTileKV;
+  float* red = reinterpret_cast<float*>(smem + kRedOffset);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -280,13 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid / 32;
   const int lane = tid % 32;
   const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-  if (tid == 32 && p.paged && n_tiles > 0) {
-    // warm the first block-table entries the producer needs, while the CTA sets up
-    uint32_t warm;
-    const int blk0 = j0 * kBN / p.block_size;
-    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(warm) : "l"(table + blk0) : "memory");
-    if (n_tiles > 1) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(warm) : "l"(table + (j0 + 1) * kBN / p.block_size) : "memory");
-  }
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -299,12 +296,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[S_FULL + x], 1);
-      mbar_init(&bars[P_FULL + x], kSoftmaxWarps);
+      mbar_init(&bars[P_FULL + x], kSoftmaxWarps);  // one arrival per softmax warp
       mbar_init(&bars[O_DONE + x], 1);
     }
     mbar_init(&bars[O_FINAL], 1);
+    mbar_init(&bars[O_FINAL + 1], 1);
     mbar_init(&bars[V_TAIL], 1);
     fence_mbar_init();
+  }
+  const Waiter wait{abort_flag, p.err};
+  // Loads tile j's K (is_v = false) or V into stage j % kStages, after the
+  // stage's previous occupant (tile j - kStages) was released.
+  auto load_tile = [&](int j, bool is_v) {
+    const int st = j % kStages;
+    const int use = j / kStages;
+    uint64_t* full = &bars[(is_v ? V_FULL : K_FULL) + st];
+    if (use > 0) wait(&bars[(is_v ? V_EMPTY : K_EMPTY) + st], (use - 1) & 1);
+    unsigned char* dst = (is_v ? sv : sk) + st * kTileKV;
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    const int key0 = (j0 + j) * kBN;
+    if (p.paged) {
+      const uint32_t piece_bytes = p.piece_rows * 128u;
+      for (int r = 0; r < kBN; r += p.piece_rows) {
+        const int key = key0 + r;
+        if (key >= nk) break;
+        const int blk = key / p.block_size;
+        const int phys = __ldg(table + blk);
+        if (phys < 0 || phys >= p.num_blocks) {
+          raise_error(p.err, PKV_DERR_BLOCK_RANGE);
+          continue;
+        }
+        const int row = phys * p.block_size + (key - blk * p.block_size);
+        mbar_expect_tx(full, 2 * piece_bytes);
+        tc::tma_load_3d(dst + r * 128, map, 0, g, row, full);
+        tc::tma_load_3d(dst + kSlabKV + r * 128, map, 64, g, row, full);
+      }
+    } else {
+      const int row = k_begin + key0;
+      mbar_expect_tx(full, kTileKV);
+      tc::tma_load_3d(dst, map, 0, g, row, full);
+      tc::tma_load_3d(dst + kSlabKV, map, 64, g, row, full);
+    }
+    mbar_arrive(full);
+  };
+  // the producer thread issues Q and the first K/V tiles (stages still free)
+  // before the CTA-wide sync, so their latency overlaps the TMEM allocation
+  const int n_early = min(n_tiles, kStages);
+  if (tid == 0) {
+    tc::prefetch_tensormap(&tm_q);
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_v);
+    const int nx = n_b > 0 ? 2 : 1;
+    mbar_expect_tx(&bars[Q_FULL], nx * kTileQ);
+    for (int x = 0; x < nx; ++x) {
+      tc::tma_load_3d(sq + x * kTileQ, &tm_q, 0, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
+      tc::tma_load_3d(sq + x * kTileQ + kSlabQ, &tm_q, 64, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
+    }
+    mbar_arrive(&bars[Q_FULL]);
+    for (int j = 0; j < n_early; ++j) {
+      load_tile(j, false);
+      load_tile(j, true);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -315,61 +367,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
-  const Waiter wait{abort_flag, p.err};
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tc::prefetch_tensormap(&tm_q);
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
-      const int nx = n_b > 0 ? 2 : 1;
-      mbar_expect_tx(&bars[Q_FULL], nx * kTileQ);
-      for (int x = 0; x < nx; ++x) {
-        tc::tma_load_3d(sq + x * kTileQ, &tm_q, 0, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
-        tc::tma_load_3d(sq + x * kTileQ + kSlabQ, &tm_q, 64, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
-      }
-      mbar_arrive(&bars[Q_FULL]);
-      // Loads tile j's K (is_v = false) or V into stage j % kStages, after the
-      // stage's previous occupant (tile j - kStages) was released.
-      auto load_tile = [&](int j, bool is_v) {
-        const int st = j % kStages;
-        const int use = j / kStages;
-        uint64_t* full = &bars[(is_v ? V_FULL : K_FULL) + st];
-        if (use > 0) wait(&bars[(is_v ? V_EMPTY : K_EMPTY) + st], (use - 1) & 1);
-        unsigned char* dst = (is_v ? sv : sk) + st * kTileKV;
-        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-        const int key0 = (j0 + j) * kBN;
-        if (p.paged) {
-          const uint32_t piece_bytes = p.piece_rows * 128u;
-          for (int r = 0; r < kBN; r += p.piece_rows) {
-            const int key = key0 + r;
-            if (key >= nk) break;
-            const int blk = key / p.block_size;
-            const int phys = __ldg(table + blk);
-            if (phys < 0 || phys >= p.num_blocks) {
-              raise_error(p.err, PKV_DERR_BLOCK_RANGE);
-              continue;
-            }
-            const int row = phys * p.block_size + (key - blk * p.block_size);
-            mbar_expect_tx(full, 2 * piece_bytes);
-            tc::tma_load_3d(dst + r * 128, map, 0, g, row, full);
-            tc::tma_load_3d(dst + kSlabKV + r * 128, map, 64, g, row, full);
-          }
-        } else {
-          const int row = k_begin + key0;
-          mbar_expect_tx(full, kTileKV);
-          tc::tma_load_3d(dst, map, 0, g, row, full);
-          tc::tma_load_3d(dst + kSlabKV, map, 64, g, row, full);
-        }
-        mbar_arrive(full);
-      };
       // K(j) once the K stage is free (both Q K^T of tile j - 2 read it), V(j)
       // once the V stage is
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = n_early; j < n_tiles; ++j) {
         load_tile(j, false);
         load_tile(j, true);
       }
+    }
+    __syncwarp();  // every load issued before the warp turns to the last tile
+    if (v_tail) {
+      // In the last tile the V rows past nk hold whatever their block had there
+      // (or were not loaded): zero them so 0 * stale never reaches O.  Every
+      // load has been issued, so the stage's barrier is at the last tile's
+      // phase or just past it, and a parity wait for that phase is exact.
+      const int j = n_tiles - 1;
+      const int st = j % kStages;
+      wait(&bars[V_FULL + st], (j / kStages) & 1);
+      unsigned char* vt = sv + st * kTileKV;
+      const int first = nk - (j0 + j) * kBN;
+      for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
+        const int rr = first + idx / 16;
+        const int ch = idx % 16;
+        *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[V_TAIL]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -397,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_X += P_X(j) V(j)
       auto issue_pv = [&](int x, int j) {
         const int st = j % kStages;
-        wait(&bars[P_FULL + x], j & 1);
+        wait.ready(&bars[P_FULL + x], j & 1);
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -415,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n_x[x] > 0) issue_qk(x, 0);
         tc::commit(&bars[K_EMPTY]);
       }
+      for (int x = 0; x < 2; ++x)
+        if (n_x[x] == 0) tc::commit(&bars[O_FINAL + x]);  // a tile with no key tile here: nothing to wait for
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kStages;
         if (v_tail && j == n_tiles - 1)
@@ -424,7 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool next = j + 1 < n_tiles;
         bool k_next = false;  // K(j + 1) seen loaded
         for (int x = 0; x < 2; ++x) {
-          if (j < n_x[x]) issue_pv(x, j);
+          if (j < n_x[x]) {
+            issue_pv(x, j);
+            if (j == n_x[x] - 1) tc::commit(&bars[O_FINAL + x]);
+          }
           if (j + 1 < n_x[x]) {
             if (!k_next) {
               wait.ready(&bars[K_FULL + (j + 1) % kStages], ((j + 1) / kStages) & 1);
@@ -437,121 +469,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&bars[V_EMPTY + st]);
         if (next) tc::commit(&bars[K_EMPTY + (j + 1) % kStages]);
       }
-      tc::commit(&bars[O_FINAL]);
-      // no MMA may be in flight when TMEM is freed
-      wait(&bars[O_FINAL], 0);
-    }
-  } else if (warp == kGuardWarp) {
-    // ------------------------------------------------------------ V guard
-    // In the last tile the V rows past nk hold whatever their block had there
-    // (or were not loaded): zero them so 0 * stale never reaches O.
-    if (v_tail) {
-      const int j = n_tiles - 1;
-      const int st = j % kStages;
-      // follow the stage's phases in order up to the last tile's: a parity wait
-      // for a phase two or more ahead would return at once
-      for (int t = st; t <= j; t += kStages) wait(&bars[V_FULL + st], (t / kStages) & 1);
-      unsigned char* vt = sv + st * kTileKV;
-      const int first = nk - (j0 + j) * kBN;
-      for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
-        const int rr = first + idx / 16;
-        const int ch = idx % 16;
-        *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[V_TAIL]);
+      // no MMA may be in flight when TMEM is freed: tile B's last product (or
+      // A's, when B has none here) is the last MMA issued
+      wait(&bars[O_FINAL + (n_b > 0 ? 1 : 0)], 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax + epilogue of tile X
+    // ------------------------------------------------------------ softmax + epilogue of tile X, one half of the keys
     const int x = (warp - 2) / kSoftmaxWarps;
+    const int half = ((warp - 2) % kSoftmaxWarps) / 4;
     const int n_x = x == 0 ? n_a : n_b;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    const int gt = half * kBM + row;  // 0..255 within the tile's softmax threads
     const int tok_first = tok0 + x * TQ;  // first token of this query tile
     const int tok = tok_first + row / G;
-    const int head = row % G;
     const int pos = cached + tok;  // absolute position of this query row
-    const bool row_valid = tok < nq;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + x * kBN;
-    const uint32_t o_addr = lane_addr + kColO + x * kD;
+    const uint32_t o_addr = lane_addr + kColO + x * kD + half * 64;  // this half's 64 output columns
     const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
+    const int bar_id = 1 + x;
+    constexpr int kGroup = 32 * kSoftmaxWarps;
+    auto red_at = [&](int parity, int h) { return red + ((parity * 2 + x) * 2 + h) * kBM + row; };
     float m_run = -INFINITY;
-    float l_run = 0.f;
-    uint32_t r[32];
+    float l_run = 0.f;  // this half's keys only
+    uint32_t r[64];
 
     for (int j = 0; j < n_x; ++j) {
-      const int key0 = (j0 + j) * kBN;
+      const int key0 = (j0 + j) * kBN + half * 64;  // first key of this half
       wait(&bars[S_FULL + x], j & 1);
       tc::fence_after_sync();
-      const bool masked = key0 + kBN - 1 > (p.causal ? cached + tok_first : nk - 1);
-      // pass 1: row maximum of the raw scores (the scale, > 0, is applied
-      // after), 32 columns at a time, as four chains of three-input maxima
+      // this half's 64 scores, held in registers: the other half writes its P
+      // over them once both halves have exchanged their maxima
+      tc::tmem_ld32(s_addr + half * 64, r);
+      tc::tmem_ld32(s_addr + half * 64 + 32, r + 32);
+      tc::tmem_wait_ld();
+      if (key0 + 63 > (p.causal ? cached + tok_first : nk - 1)) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (key0 + e > lim) r[e] = __float_as_uint(-INFINITY);
+      }
+      // raw-score maximum of this half (the scale, > 0, is applied after), as
+      // four chains of three-input maxima; then the row's, through shared memory
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        tc::tmem_ld32(s_addr + c * 32, r);
-        tc::tmem_wait_ld();
-        if (masked) {
+      for (int e = 0; e < 64; e += 8) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + c * 32 + e > lim) r[e] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mx[u] = max3(mx[u], __uint_as_float(r[e + 2 * u]), __uint_as_float(r[e + 2 * u + 1]));
-        }
+        for (int u = 0; u < 4; ++u)
+          mx[u] = max3(mx[u], __uint_as_float(r[e + 2 * u]), __uint_as_float(r[e + 2 * u + 1]));
       }
-      const float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      *red_at(j & 1, half) = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      named_barrier_sync(bar_id, kGroup);
+      const float mt = fmaxf(*red_at(j & 1, 0), *red_at(j & 1, 1));
       const float m_new = fmaxf(m_run, mt * p.scale_log2);
       const bool grow = m_new > m_run + kRescaleLog2 || (m_run == -INFINITY && m_new != -INFINITY);
-      const bool rescale = __any_sync(0xffffffffu, grow);
+      const bool rescale = __any_sync(0xffffffffu, grow);  // the same in both halves' warps
       float factor = 1.f;
       if (rescale) {
         factor = (m_run == -INFINITY || m_new <= m_run) ? 1.f : exp2f(m_run - m_new);
         m_run = fmaxf(m_run, m_new);
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      // pass 2: P = exp2(scale * s - m) rounded to bf16, packed two per column
-      // over the first half of S (chunk c's 16 columns overwrite scores that
-      // earlier chunks already consumed); the row sum adds the same rounded
-      // values (four accumulators of two lanes, so the adds do not form one
-      // long chain)
-      uint64_t l_pair[4] = {0, 0, 0, 0};
+      // P = exp2(scale * s - m) rounded to bf16, packed two per column: keys
+      // half*64 .. half*64 + 63 are P columns half*32 .. half*32 + 31 of S.  The
+      // row sum adds the same rounded values (two accumulators of two lanes,
+      // so the adds do not form one long chain)
+      uint64_t l_pair[2] = {0, 0};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        tc::tmem_ld32(s_addr + c * 32, r);
-        tc::tmem_wait_ld();
-        if (masked) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + c * 32 + e > lim) r[e] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t w = exp2_pair_bf16(r[2 * e], r[2 * e + 1], p.scale_log2, -m_use);
-          add_bf16x2(l_pair[e % 4], w);
-          r[e] = w;
-        }
-        tc::tmem_st16(s_addr + c * 16, r);
+      for (int e = 0; e < 32; ++e) {
+        const uint32_t w = exp2_pair_bf16(r[2 * e], r[2 * e + 1], p.scale_log2, -m_use);
+        add_bf16x2(l_pair[e % 2], w);
+        r[e] = w;
       }
+      tc::tmem_st32(s_addr + half * 32, r);
       float l_tile = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 2; ++u)
         l_tile += __uint_as_float(static_cast<uint32_t>(l_pair[u])) +
                   __uint_as_float(static_cast<uint32_t>(l_pair[u] >> 32));
       l_run = l_run * factor + l_tile;
       if (rescale && j > 0) {
         // O_X holds the products up to tile j-1 (complete: S_X(j) was written
-        // after P_X(j-1) V); bring it to the new maximum
+        // after P_X(j-1) V); bring this half's columns to the new maximum
         wait(&bars[O_DONE + x], (j - 1) & 1);
         tc::fence_after_sync();
         uint32_t o[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
@@ -565,11 +569,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[P_FULL + x]);
     }
 
-    wait(&bars[O_FINAL], 0);
+    wait(&bars[O_FINAL + x], 0);
     tc::fence_after_sync();
-    __nv_bfloat16* dst =
-        p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + head) * kD;
-    // this thread's 128 outputs, 32 at a time: TMEM O (zero when the tile saw no key in this part)
+    // the row sum over both halves (the exchange buffers are free: every tile's
+    // maxima were read before the last P_FULL)
+    *red_at(0, half) = l_run;
+    named_barrier_sync(bar_id, kGroup);
+    l_run = *red_at(0, 0) + *red_at(0, 1);
+    // this thread's 64 outputs, 32 at a time: TMEM O (zero when the tile saw no key in this part)
     auto load_o = [&](int c, uint32_t* o) {
       if (n_x > 0) {
         tc::tmem_ld32(o_addr + c * 32, o);
@@ -587,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       unsigned char* stage = sq + x * kTileQ;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         load_o(c, o);
 #pragma unroll
@@ -595,16 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
-          const int chunk = (c * 32 + e) / 8;
+          const int chunk = half * 8 + (c * 32 + e) / 8;
           *reinterpret_cast<uint4*>(stage + row * 256 + ((chunk ^ (row & 15)) << 4)) = Chunk<__nv_bfloat16>::pack(f);
         }
       }
-      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
-      const int t = row;  // 0..127 within the tile's softmax warps
+      named_barrier_sync(bar_id, kGroup);
 #pragma unroll 4
-      for (int k = 0; k < kBM / 8; ++k) {
-        const int rr = k * 8 + t / 16;
-        const int chunk = t % 16;
+      for (int k = 0; k < kBM * 16 / kGroup; ++k) {
+        const int rr = k * (kGroup / 16) + gt / 16;
+        const int chunk = gt % 16;
         const int tk = tok_first + rr / G;
         if (tk < nq) {
           const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + ((chunk ^ (rr & 15)) << 4));
@@ -614,30 +620,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (tok_first < nq) {
       // Split tile: every part but the last to finish publishes O (unnormalised),
-      // m and l of each row; the last waits for those records and merges.
+      // m and l of each row; the last waits for those records and merges.  Each
+      // half handles its 64 columns.
+      const bool row_valid = tok < nq;
+      __nv_bfloat16* dst = p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + row % G) * kD +
+                           half * 64;
       const int qt = 2 * pt + x;
       const long long item = (static_cast<long long>(seq) * p.hkv + g) * p.q_tiles + qt;
-      const int leader = 64 + x * 32 * kSoftmaxWarps;  // first thread of this tile's softmax warps
+      const int leader = 64 + x * kGroup;  // first thread of this tile's softmax warps
       auto record = [&](int q) {
         return reinterpret_cast<float*>(p.records + (static_cast<size_t>(item) * p.parts_max + q) * kRecordBytes);
       };
-      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+      named_barrier_sync(bar_id, kGroup);
       if (threadIdx.x == leader) s_ticket[x] = atomicAdd(p.tickets + item, 1);
-      named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+      named_barrier_sync(bar_id, kGroup);
       if (s_ticket[x] < parts - 1) {
         float* rec = record(part);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           load_o(c, o);
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            reinterpret_cast<uint4*>(rec + row * kD + c * 32 + e)[0] = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            reinterpret_cast<uint4*>(rec + row * kD + half * 64 + c * 32 + e)[0] =
+                make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
-        rec[kBM * kD + row] = m_run;
-        rec[kBM * kD + kBM + row] = l_run;
+        if (half == 0) {
+          rec[kBM * kD + row] = m_run;
+          rec[kBM * kD + kBM + row] = l_run;
+        }
         __threadfence();
-        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+        named_barrier_sync(bar_id, kGroup);
         if (threadIdx.x == leader) atomicAdd(p.ready + item, 1);
       } else {
         if (threadIdx.x == leader) {
@@ -658,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) raise_error(p.err, PKV_DERR_WAIT_TIMEOUT);
           s_ticket[x] = ok ? 1 : -1;
         }
-        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+        named_barrier_sync(bar_id, kGroup);
         __threadfence();
         if (s_ticket[x] == 1) {
           // log-sum-exp merge over the parts that saw a key of this row, in part
@@ -683,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float inv = total > 0.f ? 1.f / total : 0.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
             load_o(c, o);
             if (row_valid) {
@@ -699,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 8; ++u) v8[u] = __uint_as_float(o[e + u]);
                   } else {
-                    const float* src = record(q) + row * kD + c * 32 + e;
+                    const float* src = record(q) + row * kD + half * 64 + c * 32 + e;
                     const float4 r0 = __ldcg(reinterpret_cast<const float4*>(src));
                     const float4 r1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
                     v8[0] = r0.x, v8[1] = r0.y, v8[2] = r0.z, v8[3] = r0.w;
@@ -715,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_barrier_sync(1 + x, 32 * kSoftmaxWarps);
+        named_barrier_sync(bar_id, kGroup);
         if (threadIdx.x == leader) {  // leave the tile's slots ready for the next call
           p.tickets[item] = 0;
           p.ready[item] = 0;

@@ -107,7 +107,8 @@ def run_decode(w: wl.DecodeWorkload, *, num_splits: int = 0, poison: bool = Fals
     out = pkv.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], gm["block_tables"], gm["context_lens"],
                                 w.scale, num_splits=num_splits)
     torch.cuda.synchronize()
-    assert pkv.device_error() == 0
+    err = pkv.device_error()
+    assert err == 0, f"device error bits {err:#x}"
 
     ometa = oracle_decode_tables(w)
     assert np.array_equal(ometa["slot_mapping"], meta["slot_mapping"])
@@ -141,7 +142,8 @@ def run_prefill(w: wl.PrefillWorkload, *, use_tables: bool = True, poison: bool 
                                             meta["max_seqlen_k"], w.scale, k=g["k"], v=g["v"], causal=causal,
                                             workspace=workspace)
     torch.cuda.synchronize()
-    assert pkv.device_error() == 0
+    err = pkv.device_error()
+    assert err == 0, f"device error bits {err:#x}"
 
     seqs = [dict(block_table=tb, num_cached_tokens=c, num_scheduled_tokens=n)
             for tb, c, n in zip(w.block_tables, w.num_cached, w.num_new)]
@@ -188,7 +190,8 @@ def decode_layer_full(pool, w: wl.DecodeWorkload, layer: int, label: str) -> dic
     out = pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], gm["block_tables"], gm["context_lens"], w.scale,
                                 workspace=ws)
     torch.cuda.synchronize()
-    assert pkv.device_error() == 0
+    err = pkv.device_error()
+    assert err == 0, f"device error bits {err:#x}"
     ometa = oracle_decode_tables(w)
     assert np.array_equal(ometa["slot_mapping"], meta["slot_mapping"])
     kc_bits, vc_bits = oa.kv_store(kb_pre, vb_pre, bits(t["k_new"]), bits(t["v_new"]), ometa["slot_mapping"])

@@ -60,9 +60,9 @@ def test_prefill_workspace_is_zero_when_nothing_splits():
 
 @pytest.mark.gpu
 def test_prefill_workspace_size_rule():
-    # work items are pairs of query tiles of 128 / G tokens, one CTA per SM: P = ceil(SMs / pairs) parts
-    # (at most 8) when the pairs are fewer than the SMs; then one int ticket and one int ready count per
-    # (sequence, KV head, query tile), each array padded to 256 bytes, and P records of
+    # work items are pairs of query tiles of 128 / G tokens, one CTA per SM: P = floor(SMs / pairs) parts
+    # (at most 8, one wave) when at most half the SMs have a pair; then one int ticket and one int ready
+    # count per (sequence, KV head, query tile), each array padded to 256 bytes, and P records of
     # 128 rows x (128 fp32 + m + l) per query tile
     lib = _lib.load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -70,9 +70,9 @@ def test_prefill_workspace_size_rule():
     def expect(batch, hq, hkv, max_q):
         tq = 128 // (hq // hkv)
         pairs = batch * hkv * (-(-max_q // (2 * tq)))
-        if pairs >= sms:
+        if 2 * pairs > sms:
             return 0
-        parts = min(8, -(-sms // pairs))
+        parts = min(8, sms // pairs)
         items = 2 * pairs
         flags = -(-items * 4 // 256) * 256
         return 2 * flags + items * parts * (128 * 128 * 4 + 128 * 8)

@@ -144,8 +144,8 @@ def test_split_workspace_reused_and_left_zeroed():
 
 
 def test_single_long_history_runs_as_eight_parts():
-    # one sequence, a 16k-token history and 200 new tokens: 32 work items for a GPU with ~300 CTA slots,
-    # so each query tile (130 key tiles of 128) runs as eight parts
+    # one sequence, a 16k-token history and 200 new tokens: 16 pairs of query tiles for a GPU of ~150 SMs,
+    # so each pair (130 key tiles of 128) runs as eight parts
     w = wl.random_prefill(37, batch=1, max_new=200, min_new=200, max_cached_blocks=64, block_size=256,
                           num_q_heads=16, num_kv_heads=8, head_dim=128)
     w.num_cached[0] = 64 * 256
