@@ -195,8 +195,8 @@ class ClockSampler:
                 "samples": len(inside), "window": scope, "reasons": sorted(reasons)}
 
 
-DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh",
-                  "decode_launch.cuh", "common.cuh")
+DECODE_SOURCES = ("decode.cu", "decode_plan.cuh", "decode_simt.cuh", "decode_mma.cuh", "decode_launch.cuh",
+                  "common.cuh")
 
 
 def decode_sources_sha256() -> str:

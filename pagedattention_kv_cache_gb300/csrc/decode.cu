@@ -8,8 +8,8 @@
 // with K_t / V_t at physical block block_tables[b, t / bs], offset t % bs.
 // context_lens 0 writes zeros and reads nothing.
 //
-// How (GB300 design; the kernels are in decode_kernel.cuh and the files it
-// includes):
+// How (GB300 design; the kernels are in decode_mma.cuh and decode_simt.cuh,
+// launched from decode_launch.cuh):
 //  * A CTA covers every KV head of a token range, so each token's K (or V)
 //    row of all heads, [Hkv, D], is contiguous in the [blocks, bs, Hkv, D]
 //    pool.  A producer warp streams the range into a ring of shared-memory
@@ -26,7 +26,7 @@
 //    directly; otherwise each part writes (o, m, l) to the workspace and
 //    atomic tickets (no waiting) elect the CTAs that merge the parts by
 //    log-sum-exp, in groups of eight consecutive parts and then the groups.
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 
 extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                                    int32_t num_splits) {

@@ -70,6 +70,16 @@ __global__ void __launch_bounds__(288, 1)
     paged_decode_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
   pkv::pdl_enter();
+  {
+    // the producer reads its block-table entries right after the plan: warm
+    // L2 with the tables (when they are small) while the plan reads the lengths
+    const size_t lines = (static_cast<size_t>(p.batch) * p.max_blocks * 4 + 127) / 128;
+    if (lines <= 512) {
+      const char* tb = reinterpret_cast<const char*>(p.block_tables);
+      for (size_t i = threadIdx.x; i < lines; i += blockDim.x)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + i * 128) : "memory");
+    }
+  }
   using T = __nv_bfloat16;
   constexpr bool kFp8 = std::is_same<TC, __nv_fp8_e4m3>::value;
   constexpr int ES = static_cast<int>(sizeof(TC));  // bytes per cache element

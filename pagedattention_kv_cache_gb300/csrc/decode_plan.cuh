@@ -137,6 +137,42 @@ __device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
   const int A = align_tokens(p);
+  const long long grid = gridDim.x;
+  if (p.batch <= nthreads) {
+    // one pass when the batch fits the block: each thread loads one length,
+    // one block-wide scan gives the total and the prefix that holds `start`
+    const long long n = tid < p.batch ? round_up(context_len(p, tid), A) : 0;
+    long long incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid % 32 >= off) incl += y;
+    }
+    if (tid % 32 == 31) sh[tid / 32] = incl;
+    if (tid == 0) sh[32] = -1;
+    __syncthreads();
+    long long warp_prefix = 0;
+    long long total = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      if (w < tid / 32) warp_prefix += sh[w];
+      total += sh[w];
+    }
+    long long per = round_up((total + grid - 1) / grid, A);
+    if (per < kMinTokensPerCta) per = round_up(kMinTokensPerCta, A);
+    plan.per = per;
+    plan.start = per * blockIdx.x;
+    plan.end = plan.start + per < total ? plan.start + per : total;
+    const long long excl = warp_prefix + incl - n;
+    if (n > 0 && excl <= plan.start && plan.start < excl + n) {
+      sh[32] = tid;
+      sh[33] = excl;
+    }
+    __syncthreads();
+    plan.b_first = plan.start < plan.end ? static_cast<int>(sh[32]) : -1;
+    plan.cu_first = plan.b_first >= 0 ? sh[33] : 0;
+    __syncthreads();
+    return;
+  }
   long long local = 0;
   for (int b = tid; b < p.batch; b += nthreads) local += round_up(context_len(p, b), A);
 #pragma unroll
@@ -146,7 +182,6 @@ __device__ void plan_auto(const Params& p, Plan& plan, long long* sh) {
   long long total = 0;
   for (int w = 0; w < nthreads / 32; ++w) total += sh[w];
   __syncthreads();
-  const long long grid = gridDim.x;
   long long per = round_up((total + grid - 1) / grid, A);
   if (per < kMinTokensPerCta) per = round_up(kMinTokensPerCta, A);
   plan.per = per;

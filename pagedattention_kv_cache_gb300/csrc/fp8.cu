@@ -7,7 +7,7 @@
 // per-tensor scale per K and per V: an element x is stored as
 // e4m3(x / scale), rounded to nearest even and saturated to +-448, and read
 // back as value(code) * scale.  Decode streams half the bytes of bf16.
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 
 namespace {
 

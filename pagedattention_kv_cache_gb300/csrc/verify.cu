@@ -4,10 +4,10 @@
 // has q_len query tokens, the last q_len tokens of its context (stored first,
 // like decode's new token); query token i attends the cache up to its own
 // position context_lens[b] - q_len + i.  It is decode with q_len query rows
-// per sequence and runs on the same kernel (decode_kernel.cuh): K and V are
+// per sequence and runs on the same kernel (decode_mma.cuh): K and V are
 // streamed once per KV head for all q_len x G rows, with the same split over
 // the context and log-sum-exp combine.
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 
 namespace {
 
