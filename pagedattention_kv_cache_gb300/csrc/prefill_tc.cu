@@ -78,10 +78,10 @@ constexpr size_t kRecordBytes = static_cast<size_t>(kBM) * kD * 4 + static_cast<
 constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the last part's wait for the records
 
 // Per query tile X (A = 0, B = 1): S_FULL + X completes when S_X holds the
-// scores of the next key tile, P_FULL + X when its softmax warps have written
-// P over it, O_DONE + X once per P_X V product (waited at most one phase
-// behind, by the lazy rescale).  O_FINAL + X completes once, after the last
-// P_X V: tile X's epilogue waits on it (A's can start while B still runs).  K and V stages are released
+// scores of the next key tile (and so every P_X V issued before it has
+// completed too), P_FULL + X when its softmax warps have written P over it.
+// O_FINAL + X completes once, after the last P_X V: tile X's epilogue waits on
+// it (A's can start while B still runs).  K and V stages are released
 // separately, a K stage once both Q K^T products have read it, a V stage once
 // both P V products have.  V_TAIL: the last V tile, once its rows past the
 // last key are zeroed (only when that tile is partial).
@@ -93,8 +93,7 @@ enum Bar {
   V_EMPTY = K_EMPTY + kStages,
   S_FULL = V_EMPTY + kStages,
   P_FULL = S_FULL + 2,
-  O_DONE = P_FULL + 2,
-  O_FINAL = O_DONE + 2,  // per query tile
+  O_FINAL = P_FULL + 2,  // per query tile
   V_TAIL = O_FINAL + 2,
   NUM_BARS
 };
@@ -297,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[S_FULL + x], 1);
       mbar_init(&bars[P_FULL + x], kSoftmaxWarps);  // one arrival per softmax warp
-      mbar_init(&bars[O_DONE + x], 1);
     }
     mbar_init(&bars[O_FINAL], 1);
     mbar_init(&bars[O_FINAL + 1], 1);
@@ -371,6 +369,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      if (parts > 1) {
+        // a split part streams a key range no other CTA reads: request it into
+        // L2 first, so that the ring's loads, which start only as stages free
+        // up, find it there
+        for (int j = n_early; j < n_tiles; ++j) {
+          const int key0 = (j0 + j) * kBN;
+          for (int r = 0; r < kBN; r += p.piece_rows) {
+            const int key = key0 + r;
+            if (key >= nk) break;
+            int row = k_begin + key;
+            if (p.paged) {
+              const int blk = key / p.block_size;
+              const int phys = __ldg(table + blk);
+              if (phys < 0 || phys >= p.num_blocks) continue;  // raised by the load
+              row = phys * p.block_size + (key - blk * p.block_size);
+            }
+            tc::tma_prefetch_3d(&tm_k, 0, g, row);
+            tc::tma_prefetch_3d(&tm_k, 64, g, row);
+            tc::tma_prefetch_3d(&tm_v, 0, g, row);
+            tc::tma_prefetch_3d(&tm_v, 64, g, row);
+          }
+        }
+      }
       // K(j) once the K stage is free (both Q K^T of tile j - 2 read it), V(j)
       // once the V stage is
       for (int j = n_early; j < n_tiles; ++j) {
@@ -432,7 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_ts(tmem + kColO + x * kD, tmem + kColS + x * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::commit(&bars[O_DONE + x]);
       };
       wait(&bars[Q_FULL], 0);
       if (n_tiles > 0) {
@@ -456,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < n_x[x]) {
             issue_pv(x, j);
             if (j == n_x[x] - 1) tc::commit(&bars[O_FINAL + x]);
+            // the step's last P V (tile B's, or A's when B has no tile j) releases V(j)
+            if (x == 1 || j >= n_x[1]) tc::commit(&bars[V_EMPTY + st]);
           }
           if (j + 1 < n_x[x]) {
             if (!k_next) {
@@ -466,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_qk(x, j + 1);
           }
         }
-        tc::commit(&bars[V_EMPTY + st]);
         if (next) tc::commit(&bars[K_EMPTY + (j + 1) % kStages]);
       }
       // no MMA may be in flight when TMEM is freed: tile B's last product (or
@@ -549,10 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __uint_as_float(static_cast<uint32_t>(l_pair[u] >> 32));
       l_run = l_run * factor + l_tile;
       if (rescale && j > 0) {
-        // O_X holds the products up to tile j-1 (complete: S_X(j) was written
-        // after P_X(j-1) V); bring this half's columns to the new maximum
-        wait(&bars[O_DONE + x], (j - 1) & 1);
-        tc::fence_after_sync();
+        // O_X holds the products up to tile j-1, complete: the S_X(j) commit
+        // waited on above came after them; bring this half's columns to the new
+        // maximum before P_X(j) V is issued
         uint32_t o[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
