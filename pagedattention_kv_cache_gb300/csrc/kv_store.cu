@@ -17,59 +17,52 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-// A token row (all KV heads of the token) is cpr 16-byte chunks.  Lanes are
-// grouped per token: a group of lpt lanes (cpr rounded up to a power of two,
-// at most 32) takes one piece of kb * lpt chunks of a token, each lane kb
-// (<= kBatch) of them.  The slot and every chunk of the piece are loaded
-// before anything is stored, so one round trip to memory covers it.  Small
-// batches (a decode step's few hundred tokens) take kb = 1 and several pieces
-// per row, so they still spread over the SMs.
+// A token row (all KV heads of the token) is cpr 16-byte chunks, and the
+// rows of k and v are consecutive, so the batch is one flat run of
+// num_tokens * cpr chunks: chunk c belongs to token c / cpr, at chunk c % cpr
+// of its row.  Thread t of T takes chunks t, t + T, t + 2T, ..., kBatch at a
+// time: their K and V loads (and the slots) go out before any store, so one
+// round trip to memory covers them.  Every thread's share differs from the
+// others' by at most one chunk, whatever the batch size, and consecutive
+// threads take consecutive chunks, so loads and stores stay coalesced (a
+// warp's 512 bytes cross at most one row boundary when cpr >= 32).
 constexpr int kBatch = 4;
 constexpr int kBlocksPerSm = 4;  // resident blocks of 256 threads at this kernel's register count
 
 __global__ void __launch_bounds__(256, kBlocksPerSm) kv_store_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                                       const int32_t* __restrict__ slot_mapping, int64_t units,
-                                                       int32_t pieces, int32_t cpr, int32_t lpt, int32_t kb,
-                                                       int64_t num_slots, unsigned int* err) {
+                                                       const int32_t* __restrict__ slot_mapping, int64_t chunks,
+                                                       int32_t cpr, int32_t cpr_shift, int64_t num_slots,
+                                                       unsigned int* err) {
   pkv::pdl_enter();
-  const int lane = threadIdx.x % 32;
-  const int sub = lane / lpt;  // unit of this lane inside the warp's group
-  const int cl = lane % lpt;
-  const int upw = 32 / lpt;    // units per warp pass
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
-  for (int64_t u0 = warp * upw; u0 < units; u0 += nwarps * upw) {
-    const int64_t unit = u0 + sub;
-    if (unit >= units) continue;
-    const int64_t token = unit / pieces;
-    const int c0 = static_cast<int>(unit - token * pieces) * kb * lpt + cl;  // this lane's first chunk
-    const int32_t slot = __ldg(slot_mapping + token);
-    const uint4* ks = k + token * cpr;
-    const uint4* vs = v + token * cpr;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // token of chunk c: a shift when cpr is a power of two (cpr_shift >= 0)
+  auto token_of = [&](int64_t c) { return cpr_shift >= 0 ? c >> cpr_shift : c / cpr; };
+  for (int64_t c0 = t; c0 < chunks; c0 += kBatch * nthreads) {
     uint4 kr[kBatch], vr[kBatch];
+    int32_t slot[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int c = c0 + u * lpt;
-      if (u < kb && c < cpr) {
-        kr[u] = ld_stream(ks + c);
-        vr[u] = ld_stream(vs + c);
+      const int64_t c = c0 + u * nthreads;
+      if (c < chunks) {
+        slot[u] = __ldg(slot_mapping + token_of(c));
+        kr[u] = ld_stream(k + c);
+        vr[u] = ld_stream(v + c);
       }
     }
-    if (slot == -1) continue;
-    if (slot < 0 || slot >= num_slots) {
-      if (c0 == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);
-      continue;
-    }
-    uint4* kd = k_cache + static_cast<int64_t>(slot) * cpr;
-    uint4* vd = v_cache + static_cast<int64_t>(slot) * cpr;
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int c = c0 + u * lpt;
-      if (u < kb && c < cpr) {
-        kd[c] = kr[u];
-        vd[c] = vr[u];
+      const int64_t c = c0 + u * nthreads;
+      if (c >= chunks || slot[u] == -1) continue;
+      const int64_t within = c - token_of(c) * cpr;
+      if (slot[u] < 0 || slot[u] >= num_slots) {
+        if (within == 0) pkv::raise_error(err, PKV_DERR_SLOT_RANGE);  // once per token
+        continue;
       }
+      const int64_t dst = static_cast<int64_t>(slot[u]) * cpr + within;
+      k_cache[dst] = kr[u];
+      v_cache[dst] = vr[u];
     }
   }
 }
@@ -98,21 +91,20 @@ extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v
 
   if (row_bytes / 16 > INT32_MAX) return PKV_EUNSUPPORTED;
   const int32_t cpr = static_cast<int32_t>(row_bytes / 16);
-  int32_t lpt = 1;
-  while (lpt < cpr && lpt < 32) lpt *= 2;
+  int32_t cpr_shift = -1;
+  if ((cpr & (cpr - 1)) == 0) {
+    cpr_shift = 0;
+    while ((1 << cpr_shift) < cpr) ++cpr_shift;
+  }
+  const int64_t chunks = static_cast<int64_t>(num_tokens) * cpr;
   const int threads = 256;
+  // one chunk per thread until every resident block is in use, then more per thread
   const int64_t cap = static_cast<int64_t>(info.sms) * kBlocksPerSm;
-  // kBatch chunks per lane once the batch fills every resident warp, else one
-  const int64_t units_full = static_cast<int64_t>(num_tokens) * ((cpr + kBatch * lpt - 1) / (kBatch * lpt));
-  const int32_t kb = units_full * lpt / 32 >= cap * (threads / 32) ? kBatch : 1;
-  const int32_t pieces = (cpr + kb * lpt - 1) / (kb * lpt);
-  const int64_t units = static_cast<int64_t>(num_tokens) * pieces;
-  const int64_t units_per_block = (threads / 32) * (32 / lpt);
-  int64_t blocks = (units + units_per_block - 1) / units_per_block;
+  int64_t blocks = (chunks + threads - 1) / threads;
   if (blocks > cap) blocks = cap;
   const cudaError_t e = pkv::launch_pdl(
       kv_store_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, static_cast<const uint4*>(k),
-      static_cast<const uint4*>(v), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, units,
-      pieces, cpr, lpt, kb, static_cast<int64_t>(num_blocks) * block_size, err);
+      static_cast<const uint4*>(v), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, chunks,
+      cpr, cpr_shift, static_cast<int64_t>(num_blocks) * block_size, err);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
