@@ -318,10 +318,11 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *                   on timing).  Otherwise nothing is split.  It must be zero-filled once
  *                   after allocation; every call leaves it ready for the next one.  Calls
  *                   sharing a workspace must not overlap in time.
- * Supported: BF16 only; head_dim 128; G in {1, 2, 4, 8}.  Block sizes that are a
- * multiple of 128, or a divisor of 128 of at least 8, and the packed path run on
- * the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel (which
- * ignores the workspace).
+ * Supported: BF16 only; head_dim 64 or 128; G in {1, 2, 4, 8}.  Block sizes that
+ * are a multiple of 128, or a divisor of 128 of at least 8, and the packed path run
+ * on the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel (which
+ * ignores the workspace, and takes head_dim 128 only: head_dim 64 with such a block
+ * size returns PKV_EUNSUPPORTED).
  */
 int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const void* v,
                                   const void* k_cache, const void* v_cache,

@@ -349,7 +349,7 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
       max_seqlen_q < 0 || max_seqlen_k < 0)
     return PKV_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
-  if (dtype != PKV_BF16 || head_dim != kD) return PKV_EUNSUPPORTED;
+  if (dtype != PKV_BF16 || (head_dim != kD && head_dim != 64)) return PKV_EUNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_EUNSUPPORTED;
   if (causal != 0 && causal != 1) return PKV_EINVAL;
@@ -394,9 +394,11 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
   a.scale = scale;
   a.causal = causal;
   a.group = group;
+  a.head_dim = head_dim;
   a.workspace = workspace;
   a.workspace_bytes = workspace ? workspace_bytes : 0;
   if (pkv::prefill_tc_supported(a)) return pkv::prefill_tc_launch(a, stream);
+  if (head_dim != kD) return PKV_EUNSUPPORTED;  // the mma.sync kernel below is head_dim 128 only
 
   Params p{};
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -430,6 +432,6 @@ extern "C" int pkv_paged_varlen_prefill_attn(void* out, const void* q, const voi
 
 extern "C" size_t pkv_paged_varlen_prefill_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                                           int32_t head_dim, int32_t max_seqlen_q) {
-  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim != kD) return 0;
-  return pkv::prefill_tc_workspace_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, max_seqlen_q);
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+  return pkv::prefill_tc_workspace_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, max_seqlen_q);
 }

@@ -28,17 +28,18 @@ struct PrefillArgs {
   int num_blocks;
   float scale;
   int causal;
-  int group;  // hq / hkv
+  int group;     // hq / hkv
+  int head_dim;  // 64 or 128 (the mma.sync kernel: 128 only)
   void* workspace;         // split of long items (tcgen05 path), or null
   size_t workspace_bytes;
 };
 
-// Tensor-core (tcgen05 + TMEM + TMA) path; requires head_dim 128, bf16, and
+// Tensor-core (tcgen05 + TMEM + TMA) path; requires head_dim 64 or 128, bf16, and
 // for the paged case a block size that is a multiple of 128 or a divisor of
 // 128 of at least 8.
 bool prefill_tc_supported(const PrefillArgs& a);
 int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
 // Workspace bytes that let the tcgen05 path split long items (0: never splits).
-size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int max_seqlen_q);
+size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int head_dim, int max_seqlen_q);
 
 }  // namespace pkv

@@ -44,7 +44,6 @@ namespace {
 
 using namespace pkv;
 
-constexpr int kD = 128;
 constexpr int kBM = 128;   // rows per query tile
 constexpr int kBN = 128;   // keys per tile
 constexpr int kStages = 2; // K ring and V ring depth
@@ -55,13 +54,25 @@ constexpr uint32_t kColS = 0;    // S_A at 0, S_B at 128
 constexpr uint32_t kColO = 256;  // O_A at 256, O_B at 384
 constexpr uint32_t kSlabQ = kBM * 128;
 constexpr uint32_t kSlabKV = kBN * 128;
-constexpr uint32_t kTileQ = 2 * kSlabQ;
-constexpr uint32_t kTileKV = 2 * kSlabKV;
-constexpr uint32_t kRedOffset = 2 * kTileQ + 2 * kStages * kTileKV;  // row maxima / sums exchanged by the halves
-constexpr uint32_t kRedBytes = 2 * 2 * 2 * kBM * 4;                  // [tile parity][query tile][half][row]
-constexpr uint32_t kBarOffset = kRedOffset + kRedBytes;
-constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
-static_assert(kSmemBytes <= 227 * 1024, "shared memory plan exceeds an SM");
+constexpr uint32_t kRedBytes = 2 * 2 * 2 * kBM * 4;  // row maxima / sums exchanged by the halves: [tile parity][query tile][half][row]
+
+// Sizes for head dimension D (64 or 128): a row of D bf16 is D / 64 slabs of
+// 128 bytes (one 128-byte swizzle atom each), and each slab of a tile is a
+// TMA box of its own.
+template <int D>
+struct Geo {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kSlabs = D / 64;
+  static constexpr uint32_t kTileQ = kSlabs * kSlabQ;
+  static constexpr uint32_t kTileKV = kSlabs * kSlabKV;
+  static constexpr uint32_t kRedOffset = 2 * kTileQ + 2 * kStages * kTileKV;
+  static constexpr uint32_t kBarOffset = kRedOffset + kRedBytes;
+  static constexpr uint32_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + 1 KB for alignment
+  // one CTA per SM even when two would fit (each holds all 512 TMEM columns)
+  static constexpr uint32_t kLaunchSmem = kSmemBytes > 120 * 1024 ? kSmemBytes : 120 * 1024;
+  static constexpr size_t kRecordBytes = static_cast<size_t>(kBM) * D * 4 + static_cast<size_t>(kBM) * 8;
+};
+static_assert(Geo<128>::kSmemBytes <= 227 * 1024, "shared memory plan exceeds an SM");
 constexpr float kRescaleLog2 = 8.0f;
 
 // Key-range split of long work items, used only when the pairs do not fill
@@ -74,7 +85,6 @@ constexpr float kRescaleLog2 = 8.0f;
 // order, and stores the output.
 constexpr int kSplitMinTiles = 8;
 constexpr int kMaxParts = 8;
-constexpr size_t kRecordBytes = static_cast<size_t>(kBM) * kD * 4 + static_cast<size_t>(kBM) * 8;
 constexpr uint64_t kSplitWaitNs = 1000000000ull;  // bound on the last part's wait for the records
 
 // Per query tile X (A = 0, B = 1): S_FULL + X completes when S_X holds the
@@ -121,7 +131,7 @@ struct TcParams {
   int parts_max;   // P: the most parts a long pair runs as (1: no split)
   int* tickets;    // [sequences x KV heads x q_tiles]: finish order of a split tile's parts, reset by the last
   int* ready;      // [same]: records published so far, reset by the last
-  unsigned char* records;  // [same][P][kRecordBytes]: O rows (fp32), then m[kBM], l[kBM]
+  unsigned char* records;  // [same][P][record bytes]: O rows (D fp32 each), then m[kBM], l[kBM]
 };
 
 }  // namespace
@@ -141,8 +151,9 @@ int prefill_tc_parts(int batch, int num_kv_heads, int group, int max_seqlen_q, i
 // Workspace of the tcgen05 prefill: tickets and ready counts (256-byte aligned
 // blocks), then P records per (sequence, KV head, query tile); 0 when the
 // current device's SMs are filled without splitting.
-size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int max_seqlen_q) {
+size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int head_dim, int max_seqlen_q) {
   if (batch <= 0 || num_kv_heads <= 0 || max_seqlen_q <= 0) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
   if (group != 1 && group != 2 && group != 4 && group != 8) return 0;
   DeviceInfo info;
   if (device_info(&info) != PKV_OK) return 0;
@@ -151,7 +162,8 @@ size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int ma
   const long long tq = kBM / group;
   const long long items = static_cast<long long>(batch) * num_kv_heads * 2 * ((max_seqlen_q + 2 * tq - 1) / (2 * tq));
   const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
-  return 2 * flags + static_cast<size_t>(items) * parts * kRecordBytes;
+  const size_t record = head_dim == 64 ? Geo<64>::kRecordBytes : Geo<128>::kRecordBytes;
+  return 2 * flags + static_cast<size_t>(items) * parts * record;
 }
 
 }  // namespace pkv
@@ -218,12 +230,17 @@ __device__ __forceinline__ void add_bf16x2(uint64_t& acc, uint32_t w) {
       : "r"(w));
 }
 
-template <int G>
+template <int G, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   pdl_enter();
   constexpr int TQ = kBM / G;
+  constexpr int kD = D;
+  constexpr int kSlabs = Geo<D>::kSlabs;
+  constexpr uint32_t kTileQ = Geo<D>::kTileQ;
+  constexpr uint32_t kTileKV = Geo<D>::kTileKV;
+  constexpr size_t kRecordBytes = Geo<D>::kRecordBytes;
   // blocks launch in linear order: x runs over (sequence, KV head), y over
   // query-tile pairs from the last (most keys under the causal mask) to the
   // first, and, with a workspace, over the key-range parts of each pair
@@ -273,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sq = smem;  // Q_A, then Q_B
   unsigned char* sk = sq + 2 * kTileQ;
   unsigned char* sv = sk + kStages * kTileKV;
-  float* red = reinterpret_cast<float*>(smem + kRedOffset);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  float* red = reinterpret_cast<float*>(smem + Geo<D>::kRedOffset);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<D>::kBarOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ticket = abort_flag + 1;  // split tiles' tickets, one per query tile
@@ -325,15 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const int row = phys * p.block_size + (key - blk * p.block_size);
-        mbar_expect_tx(full, 2 * piece_bytes);
+        mbar_expect_tx(full, kSlabs * piece_bytes);
         tc::tma_load_3d(dst + r * 128, map, 0, g, row, full);
-        tc::tma_load_3d(dst + kSlabKV + r * 128, map, 64, g, row, full);
+        if constexpr (kSlabs == 2) tc::tma_load_3d(dst + kSlabKV + r * 128, map, 64, g, row, full);
       }
     } else {
       const int row = k_begin + key0;
       mbar_expect_tx(full, kTileKV);
       tc::tma_load_3d(dst, map, 0, g, row, full);
-      tc::tma_load_3d(dst + kSlabKV, map, 64, g, row, full);
+      if constexpr (kSlabs == 2) tc::tma_load_3d(dst + kSlabKV, map, 64, g, row, full);
     }
     mbar_arrive(full);
   };
@@ -348,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_expect_tx(&bars[Q_FULL], nx * kTileQ);
     for (int x = 0; x < nx; ++x) {
       tc::tma_load_3d(sq + x * kTileQ, &tm_q, 0, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
-      tc::tma_load_3d(sq + x * kTileQ + kSlabQ, &tm_q, 64, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
+      if constexpr (kSlabs == 2)
+        tc::tma_load_3d(sq + x * kTileQ + kSlabQ, &tm_q, 64, g * G, q_begin + tok0 + x * TQ, &bars[Q_FULL]);
     }
     mbar_arrive(&bars[Q_FULL]);
     for (int j = 0; j < n_early; ++j) {
@@ -386,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               row = phys * p.block_size + (key - blk * p.block_size);
             }
             tc::tma_prefetch_3d(&tm_k, 0, g, row);
-            tc::tma_prefetch_3d(&tm_k, 64, g, row);
+            if constexpr (kSlabs == 2) tc::tma_prefetch_3d(&tm_k, 64, g, row);
             tc::tma_prefetch_3d(&tm_v, 0, g, row);
-            tc::tma_prefetch_3d(&tm_v, 64, g, row);
+            if constexpr (kSlabs == 2) tc::tma_prefetch_3d(&tm_v, 64, g, row);
           }
         }
       }
@@ -410,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(&bars[V_FULL + st], (j / kStages) & 1);
       unsigned char* vt = sv + st * kTileKV;
       const int first = nk - (j0 + j) * kBN;
-      for (int idx = lane; idx < (kBN - first) * 16; idx += 32) {
-        const int rr = first + idx / 16;
-        const int ch = idx % 16;
+      for (int idx = lane; idx < (kBN - first) * kSlabs * 8; idx += 32) {
+        const int rr = first + idx / (kSlabs * 8);
+        const int ch = idx % (kSlabs * 8);
         *reinterpret_cast<uint4*>(vt + (ch >> 3) * kSlabKV + rr * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -507,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = cached + tok;  // absolute position of this query row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + x * kBN;
-    const uint32_t o_addr = lane_addr + kColO + x * kD + half * 64;  // this half's 64 output columns
+    const uint32_t o_addr = lane_addr + kColO + x * kD + half * (kD / 2);  // this half's D / 2 output columns
     const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
     const int bar_id = 1 + x;
     constexpr int kGroup = 32 * kSoftmaxWarps;
@@ -575,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // maximum before P_X(j) V is issued
         uint32_t o[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kD / 64; ++c) {
           tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
@@ -608,13 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (parts == 1) {
       // normalised bf16 rows staged in this tile's Q buffer (free: every MMA has
-      // completed), 16-byte chunk c of row r at chunk position c ^ (r & 15) so
-      // the eight rows of a quarter-warp hit distinct banks; then copied out
-      // two rows (512 contiguous bytes when G > 1) per warp instruction
+      // completed), 16-byte chunk c of row r at chunk position c ^ (r mod the
+      // chunks per row) so the eight rows of a quarter-warp hit distinct banks;
+      // then copied out 512 contiguous bytes (when G > 1) per warp instruction
+      constexpr int kChunks = kD / 8;  // 16-byte chunks per row
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       unsigned char* stage = sq + x * kTileQ;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kD / 64; ++c) {
         uint32_t o[32];
         load_o(c, o);
 #pragma unroll
@@ -622,18 +641,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(o[e + u]) * inv;
-          const int chunk = half * 8 + (c * 32 + e) / 8;
-          *reinterpret_cast<uint4*>(stage + row * 256 + ((chunk ^ (row & 15)) << 4)) = Chunk<__nv_bfloat16>::pack(f);
+          const int chunk = half * (kChunks / 2) + (c * 32 + e) / 8;
+          *reinterpret_cast<uint4*>(stage + row * (kD * 2) + ((chunk ^ (row & (kChunks - 1))) << 4)) =
+              Chunk<__nv_bfloat16>::pack(f);
         }
       }
       named_barrier_sync(bar_id, kGroup);
 #pragma unroll 4
-      for (int k = 0; k < kBM * 16 / kGroup; ++k) {
-        const int rr = k * (kGroup / 16) + gt / 16;
-        const int chunk = gt % 16;
+      for (int k = 0; k < kBM * kChunks / kGroup; ++k) {
+        const int rr = k * (kGroup / kChunks) + gt / kChunks;
+        const int chunk = gt % kChunks;
         const int tk = tok_first + rr / G;
         if (tk < nq) {
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 256 + ((chunk ^ (rr & 15)) << 4));
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(stage + rr * (kD * 2) + ((chunk ^ (rr & (kChunks - 1))) << 4));
           __nv_bfloat16* o_row = p.out + (static_cast<size_t>(q_begin + tk) * p.hq + g * G + rr % G) * kD;
           reinterpret_cast<uint4*>(o_row)[chunk] = v;
         }
@@ -641,10 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (tok_first < nq) {
       // Split tile: every part but the last to finish publishes O (unnormalised),
       // m and l of each row; the last waits for those records and merges.  Each
-      // half handles its 64 columns.
+      // half handles its D / 2 columns.
       const bool row_valid = tok < nq;
       __nv_bfloat16* dst = p.out + (static_cast<size_t>(q_begin + (row_valid ? tok : 0)) * p.hq + g * G + row % G) * kD +
-                           half * 64;
+                           half * (kD / 2);
       const int qt = 2 * pt + x;
       const long long item = (static_cast<long long>(seq) * p.hkv + g) * p.q_tiles + qt;
       const int leader = 64 + x * kGroup;  // first thread of this tile's softmax warps
@@ -657,12 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s_ticket[x] < parts - 1) {
         float* rec = record(part);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kD / 64; ++c) {
           uint32_t o[32];
           load_o(c, o);
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            reinterpret_cast<uint4*>(rec + row * kD + half * 64 + c * 32 + e)[0] =
+            reinterpret_cast<uint4*>(rec + row * kD + half * (kD / 2) + c * 32 + e)[0] =
                 make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
         if (half == 0) {
@@ -716,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float inv = total > 0.f ? 1.f / total : 0.f;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < kD / 64; ++c) {
             uint32_t o[32];
             load_o(c, o);
             if (row_valid) {
@@ -732,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 8; ++u) v8[u] = __uint_as_float(o[e + u]);
                   } else {
-                    const float* src = record(q) + row * kD + half * 64 + c * 32 + e;
+                    const float* src = record(q) + row * kD + half * (kD / 2) + c * 32 + e;
                     const float4 r0 = __ldcg(reinterpret_cast<const float4*>(src));
                     const float4 r1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
                     v8[0] = r0.x, v8[1] = r0.y, v8[2] = r0.z, v8[3] = r0.w;
@@ -765,9 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int G>
+template <int G, int D>
 int launch(const PrefillArgs& a, cudaStream_t stream) {
   constexpr int TQ = kBM / G;
+  constexpr int kD = D;
   alignas(64) CUtensorMap tm_q, tm_k, tm_v;
   if (encode_bf16_3d(&tm_q, a.q, kD, a.hq, a.total_q, 64, G, TQ) != PKV_OK) return PKV_ECUDA;
   const bool paged = a.block_tables != nullptr;
@@ -800,7 +822,7 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   p.parts_max = 1;
   DeviceInfo info;
   if (device_info(&info) != PKV_OK) return PKV_ECUDA;
-  const size_t ws_need = prefill_tc_workspace_bytes(a.batch, a.hkv, G, a.max_seqlen_q);
+  const size_t ws_need = prefill_tc_workspace_bytes(a.batch, a.hkv, G, D, a.max_seqlen_q);
   if (a.workspace && ws_need > 0 && a.workspace_bytes >= ws_need) {
     const long long items = static_cast<long long>(a.batch) * a.hkv * p.q_tiles;
     const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
@@ -810,7 +832,8 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
     p.ready = reinterpret_cast<int*>(ws + flags);
     p.records = ws + 2 * flags;
   }
-  auto kernel = prefill_tc_kernel<G>;
+  auto kernel = prefill_tc_kernel<G, D>;
+  constexpr uint32_t kSmemBytes = Geo<D>::kLaunchSmem;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
       cudaSuccess)
     return PKV_ECUDA;
@@ -825,6 +848,7 @@ namespace pkv {
 
 bool prefill_tc_supported(const PrefillArgs& a) {
   if (a.group != 1 && a.group != 2 && a.group != 4 && a.group != 8) return false;
+  if (a.head_dim != 64 && a.head_dim != 128) return false;
   if (a.total_q <= 0) return false;
   if (a.block_tables) {
     const int bs = a.block_size;
@@ -838,13 +862,18 @@ bool prefill_tc_supported(const PrefillArgs& a) {
   return true;
 }
 
-int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream) {
+template <int D>
+int launch_d(const PrefillArgs& a, cudaStream_t stream) {
   switch (a.group) {
-    case 1: return launch<1>(a, stream);
-    case 2: return launch<2>(a, stream);
-    case 4: return launch<4>(a, stream);
-    default: return launch<8>(a, stream);
+    case 1: return launch<1, D>(a, stream);
+    case 2: return launch<2, D>(a, stream);
+    case 4: return launch<4, D>(a, stream);
+    default: return launch<8, D>(a, stream);
   }
+}
+
+int prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 64 ? launch_d<64>(a, stream) : launch_d<128>(a, stream);
 }
 
 }  // namespace pkv

@@ -51,7 +51,7 @@ def test_prefill_workspace_is_zero_when_nothing_splits():
     # shapes without a tensor-core path, empty batches and (without a GPU) any shape never split
     _built()
     lib = _lib.load()
-    assert lib.pkv_paged_varlen_prefill_workspace_bytes(16, 16, 8, 64, 512) == 0  # head_dim 64
+    assert lib.pkv_paged_varlen_prefill_workspace_bytes(16, 16, 8, 96, 512) == 0  # head_dim 96
     assert lib.pkv_paged_varlen_prefill_workspace_bytes(16, 48, 8, 128, 512) == 0  # G = 6 unsupported
     assert lib.pkv_paged_varlen_prefill_workspace_bytes(0, 16, 8, 128, 512) == 0
     if not torch.cuda.is_available():
@@ -197,13 +197,14 @@ def test_argument_errors_return_status():
                           2, 128, _lib.BF16, s)
     assert st == _lib.EALIGN
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
-                                           bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 64, 16, 4,
+                                           bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 96, 16, 4,
                                            ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
     assert st == _lib.EUNSUPPORTED
-    st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
-                                           bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, 128, 16, 4,
-                                           ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
-    assert st == _lib.EINVAL  # no block tables and no packed k / v
+    for d in (64, 128):
+        st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
+                                               bt.data_ptr(), 1, 1, None, 0, 1, 2, 0, 4, 2, d, 16, 4,
+                                               ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)
+        assert st == _lib.EINVAL  # no block tables and no packed k / v
     st = lib.pkv_paged_varlen_prefill_attn(q.data_ptr(), q.data_ptr(), None, None, None, None, bt.data_ptr(),
                                            bt.data_ptr(), 1, 1, None, 0, 1, -1, 0, 4, 2, 128, 16, 4,
                                            ctypes.c_float(0.1), 1, None, 0, _lib.BF16, s)

@@ -29,6 +29,26 @@ def test_prefill_groups_and_block_sizes(group, block_size):
     run_prefill(w)
 
 
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("block_size", [8, 16, 64, 256])
+def test_prefill_head_dim_64(group, block_size):
+    # one 64-wide slab per Q / K / V tile, O of 64 columns in TMEM, 128-byte staged output rows
+    w = wl.random_prefill(700 + group * 10 + block_size, batch=5, max_new=300, min_new=1, max_cached_blocks=4,
+                          block_size=block_size, num_q_heads=2 * group, num_kv_heads=2, head_dim=64)
+    run_prefill(w)
+
+
+def test_prefill_head_dim_64_packed_and_non_causal():
+    w = wl.random_prefill(731, batch=6, max_new=200, min_new=1, max_cached_blocks=0, block_size=16,
+                          num_q_heads=8, num_kv_heads=4, head_dim=64)
+    r_packed = run_prefill(w, use_tables=False)
+    r_paged = run_prefill(w, use_tables=True)
+    assert torch.equal(r_packed["out"], r_paged["out"])
+    w = wl.random_prefill(732, batch=4, max_new=90, min_new=1, max_cached_blocks=2, block_size=16,
+                          num_q_heads=8, num_kv_heads=4, head_dim=64)
+    run_prefill(w, causal=False)
+
+
 def test_prefill_edge_lengths():
     # empty sequences, single-row sequences, tile-boundary lengths
     news = [0, 1, 63, 64, 65, 128, 129, 31, 33]
@@ -141,6 +161,17 @@ def test_split_workspace_reused_and_left_zeroed():
     items = w.batch * hkv * -(-max(w.num_new) // (128 // (hq // hkv)))
     flags = -(-items * 4 // 256) * 256
     assert int(ws[: 2 * flags].count_nonzero()) == 0  # tickets and ready flags back at zero
+
+
+def test_long_items_split_head_dim_64():
+    # the split records hold 64 fp32 columns per row
+    w = wl.random_prefill(38, batch=3, max_new=300, min_new=40, max_cached_blocks=12, block_size=256,
+                          num_q_heads=16, num_kv_heads=8, head_dim=64)
+    assert pkv.prefill_workspace_bytes(3, 16, 8, 64, max(w.num_new)) > 0
+    split = run_prefill(w)
+    whole = run_prefill(w, workspace=False)
+    d = (split["out"].float() - whole["out"].float()).abs().max().item()
+    assert d <= 1.6e-2, d
 
 
 def test_single_long_history_runs_as_eight_parts():
