@@ -439,7 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (its descriptor arithmetic stays warp-uniform);
+    // one elected lane issues the MMAs and commits.
+    {
+      const bool leader = elect_one();
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
       // descriptors of the first Q, K and V slabs; later ones differ only in the
@@ -456,9 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t a_off = x * kTileQ + (kk >> 2) * kSlabQ + (kk & 3) * 32;
           const uint32_t b_off = st * kTileKV + (kk >> 2) * kSlabKV + (kk & 3) * 32;
-          tc::mma_ss(tmem + kColS + x * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
+          if (leader) tc::mma_ss(tmem + kColS + x * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
         }
-        tc::commit(&bars[S_FULL + x]);
+        if (leader) tc::commit(&bars[S_FULL + x]);
       };
       // O_X += P_X(j) V(j)
       auto issue_pv = [&](int x, int j) {
@@ -468,8 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t b_off = st * kTileKV + kk * 16 * 128;
-          tc::mma_ts(tmem + kColO + x * kD, tmem + kColS + x * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+          if (leader)
+            tc::mma_ts(tmem + kColO + x * kD, tmem + kColS + x * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
       wait(&bars[Q_FULL], 0);
@@ -478,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         for (int x = 0; x < 2; ++x)
           if (n_x[x] > 0) issue_qk(x, 0);
-        tc::commit(&bars[K_EMPTY]);
+        if (leader) tc::commit(&bars[K_EMPTY]);
       }
       for (int x = 0; x < 2; ++x)
-        if (n_x[x] == 0) tc::commit(&bars[O_FINAL + x]);  // a tile with no key tile here: nothing to wait for
+        if (leader && (n_x[x] == 0)) tc::commit(&bars[O_FINAL + x]);  // a tile with no key tile here: nothing to wait for
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kStages;
         if (v_tail && j == n_tiles - 1)
@@ -493,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
           if (j < n_x[x]) {
             issue_pv(x, j);
-            if (j == n_x[x] - 1) tc::commit(&bars[O_FINAL + x]);
+            if (leader && (j == n_x[x] - 1)) tc::commit(&bars[O_FINAL + x]);
             // the step's last P V (tile B's, or A's when B has no tile j) releases V(j)
-            if (x == 1 || j >= n_x[1]) tc::commit(&bars[V_EMPTY + st]);
+            if (leader && (x == 1 || j >= n_x[1])) tc::commit(&bars[V_EMPTY + st]);
           }
           if (j + 1 < n_x[x]) {
             if (!k_next) {
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_qk(x, j + 1);
           }
         }
-        if (next) tc::commit(&bars[K_EMPTY + (j + 1) % kStages]);
+        if (leader && next) tc::commit(&bars[K_EMPTY + (j + 1) % kStages]);
       }
       // no MMA may be in flight when TMEM is freed: tile B's last product (or
       // A's, when B has none here) is the last MMA issued
