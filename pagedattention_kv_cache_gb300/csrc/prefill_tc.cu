@@ -455,11 +455,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before: the tensor pipe runs one thread's MMAs in order)
       auto issue_qk = [&](int x, int j) {
         const int st = j % kStages;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t a_off = x * kTileQ + (kk >> 2) * kSlabQ + (kk & 3) * 32;
-          const uint32_t b_off = st * kTileKV + (kk >> 2) * kSlabKV + (kk & 3) * 32;
-          if (leader) tc::mma_ss(tmem + kColS + x * kBN, q_desc + (a_off >> 4), k_desc + (b_off >> 4), idesc_qk, kk > 0);
+        // the chain's first step: tile X's Q slab 0 and stage st's K slab 0
+        const uint64_t a0 = q_desc + ((x * kTileQ) >> 4);
+        const uint64_t b0 = k_desc + ((st * kTileKV) >> 4);
+        if (leader) {
+          if constexpr (kD == 128)
+            tc::mma_ss_k128(tmem + kColS + x * kBN, a0, b0, idesc_qk);
+          else
+            tc::mma_ss_k64(tmem + kColS + x * kBN, a0, b0, idesc_qk);
         }
         if (leader) tc::commit(&bars[S_FULL + x]);
       };
@@ -468,13 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStages;
         wait.ready(&bars[P_FULL + x], j & 1);
         tc::fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t b_off = st * kTileKV + kk * 16 * 128;
-          if (leader)
-            tc::mma_ts(tmem + kColO + x * kD, tmem + kColS + x * kBN + kk * 8, v_desc + (b_off >> 4), idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        if (leader)
+          tc::mma_ts_k128(tmem + kColO + x * kD, tmem + kColS + x * kBN, v_desc + ((st * kTileKV) >> 4), idesc_pv,
+                          j > 0 ? 1u : 0u);
       };
       wait(&bars[Q_FULL], 0);
       if (n_tiles > 0) {

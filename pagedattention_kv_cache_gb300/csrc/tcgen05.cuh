@@ -111,6 +111,58 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// A chain of MMAs into one accumulator, issued from one asm block so that the
+// issuing thread runs one instruction per MMA plus the two descriptor adds:
+// step i adds a_step(i) and b_step(i) (16-byte units) to the start addresses
+// of the first step's descriptors.  The first MMA accumulates when `acc` is
+// non-zero, the others always.
+#define PKV_MMA_STEP(OP, A_OFF, B_OFF) \
+  "add.s64 a1, %1, " #A_OFF ";\n\tadd.s64 b1, %2, " #B_OFF ";\n\t" OP " [%0], a1, b1, %3, p1;\n\t"
+#define PKV_MMA_STEP_TS(OP, A_OFF, B_OFF) \
+  "add.u32 t1, %1, " #A_OFF ";\n\tadd.s64 b1, %2, " #B_OFF ";\n\t" OP " [%0], [t1], b1, %3, p1;\n\t"
+#define PKV_MMA_SS "tcgen05.mma.cta_group::1.kind::f16"
+
+// Q K^T over K = 128: two 64-element slabs (slab stride 1024 units), 32 bytes per step.
+__device__ __forceinline__ void mma_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a1, b1;\n\t"
+      "setp.ne.b32 p0, %4, %4;\n\tsetp.eq.b32 p1, %4, %4;\n\t"
+      PKV_MMA_SS " [%0], %1, %2, %3, p0;\n\t"
+      PKV_MMA_STEP(PKV_MMA_SS, 2, 2) PKV_MMA_STEP(PKV_MMA_SS, 4, 4) PKV_MMA_STEP(PKV_MMA_SS, 6, 6)
+      PKV_MMA_STEP(PKV_MMA_SS, 1024, 1024) PKV_MMA_STEP(PKV_MMA_SS, 1026, 1026)
+      PKV_MMA_STEP(PKV_MMA_SS, 1028, 1028) PKV_MMA_STEP(PKV_MMA_SS, 1030, 1030)
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(0)
+      : "memory");
+}
+// The same over K = 64: one slab.
+__device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a1, b1;\n\t"
+      "setp.ne.b32 p0, %4, %4;\n\tsetp.eq.b32 p1, %4, %4;\n\t"
+      PKV_MMA_SS " [%0], %1, %2, %3, p0;\n\t"
+      PKV_MMA_STEP(PKV_MMA_SS, 2, 2) PKV_MMA_STEP(PKV_MMA_SS, 4, 4) PKV_MMA_STEP(PKV_MMA_SS, 6, 6)
+      "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(0)
+      : "memory");
+}
+// P V over 128 keys: A (P, bf16 pairs) from TMEM, 8 columns per 16 keys; B (V)
+// from shared memory, 16 rows of 128 bytes (128 units) per step.
+__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b1;\n\t.reg .b32 t1;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, %5, %5;\n\t"
+      PKV_MMA_SS " [%0], [%1], %2, %3, p0;\n\t"
+      PKV_MMA_STEP_TS(PKV_MMA_SS, 8, 128) PKV_MMA_STEP_TS(PKV_MMA_SS, 16, 256)
+      PKV_MMA_STEP_TS(PKV_MMA_SS, 24, 384) PKV_MMA_STEP_TS(PKV_MMA_SS, 32, 512)
+      PKV_MMA_STEP_TS(PKV_MMA_SS, 40, 640) PKV_MMA_STEP_TS(PKV_MMA_SS, 48, 768)
+      PKV_MMA_STEP_TS(PKV_MMA_SS, 56, 896)
+      "}" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc), "r"(0)
+      : "memory");
+}
+#undef PKV_MMA_STEP
+#undef PKV_MMA_STEP_TS
+#undef PKV_MMA_SS
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
