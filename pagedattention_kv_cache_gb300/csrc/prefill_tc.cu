@@ -195,19 +195,27 @@ struct Waiter {
 };
 
 // exp2(scale * s - m) for two scores (fma on the f32x2 pair, ex2.approx per
-// element), rounded to bf16 and packed low = first.
-__device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, float scale, float neg_m) {
+// element), rounded to bf16 and packed low = first; the two rounded values are
+// added to the row-sum lanes acc (widened exactly: fma by 1 in fp32).
+__device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, float scale, float neg_m,
+                                                   uint64_t& acc) {
   uint32_t out;
-  asm("{\n\t.reg .b64 x, c, m;\n\t.reg .f32 a, b;\n\t"
-      "mov.b64 x, {%1, %2};\n\t"
-      "mov.b64 c, {%3, %3};\n\t"
-      "mov.b64 m, {%4, %4};\n\t"
+  asm("{\n\t.reg .b64 x, c, m;\n\t.reg .f32 a, b, sa, sb;\n\t.reg .b16 pa, pb, one;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 c, {%4, %4};\n\t"
+      "mov.b64 m, {%5, %5};\n\t"
       "fma.rn.f32x2 x, x, c, m;\n\t"
       "mov.b64 {a, b}, x;\n\t"
       "ex2.approx.ftz.f32 a, a;\n\t"
       "ex2.approx.ftz.f32 b, b;\n\t"
-      "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
-      : "=r"(out)
+      "cvt.rn.bf16x2.f32 %0, b, a;\n\t"
+      "mov.b32 {pa, pb}, %0;\n\t"
+      "mov.b16 one, 0x3f80;\n\t"
+      "mov.b64 {sa, sb}, %1;\n\t"
+      "fma.rn.f32.bf16 sa, pa, one, sa;\n\t"
+      "fma.rn.f32.bf16 sb, pb, one, sb;\n\t"
+      "mov.b64 %1, {sa, sb};\n\t}"
+      : "=r"(out), "+l"(acc)
       : "r"(s0), "r"(s1), "f"(scale), "f"(neg_m));
   return out;
 }
@@ -217,17 +225,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// acc (two f32 lanes) += the two bf16 of w, widened exactly.
-__device__ __forceinline__ void add_bf16x2(uint64_t& acc, uint32_t w) {
-  asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 v;\n\t"
-      "shl.b32 lo, %1, 16;\n\t"
-      "and.b32 hi, %1, 0xffff0000;\n\t"
-      "mov.b64 v, {lo, hi};\n\t"
-      "add.rn.f32x2 %0, %0, v;\n\t}"
-      : "+l"(acc)
-      : "r"(w));
 }
 
 template <int G, int D>
@@ -578,11 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the adds do not form one long chain)
       uint64_t l_pair[2] = {0, 0};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const uint32_t w = exp2_pair_bf16(r[2 * e], r[2 * e + 1], p.scale_log2, -m_use);
-        add_bf16x2(l_pair[e % 2], w);
-        r[e] = w;
-      }
+      for (int e = 0; e < 32; ++e) r[e] = exp2_pair_bf16(r[2 * e], r[2 * e + 1], p.scale_log2, -m_use, l_pair[e % 2]);
       tc::tmem_st32(s_addr + half * 32, r);
       float l_tile = 0.f;
 #pragma unroll
