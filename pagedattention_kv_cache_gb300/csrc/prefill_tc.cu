@@ -15,7 +15,10 @@
 //              box per 64-wide d slab; paged tiles are gathered block piece by
 //              block piece).  Then the whole warp zeroes the V rows past the
 //              last key in the last tile before the MMA thread may use it.
-//   warp 1     MMA issuer (one thread).  Per key tile j the tensor pipe runs
+//   warp 1     MMA issuer: the whole warp runs the loop, one elected lane
+//              issues each group of MMAs from one asm block, so the issuing
+//              work stays warp-uniform and short (the warp shares its SMSP with
+//              four busy softmax warps).  Per key tile j the tensor pipe runs
 //                 P_A(j) V(j),  Q_A K(j+1)^T,  P_B(j) V(j),  Q_B K(j+1)^T
 //              (each a group of eight M=128, N=128 MMAs), so each tile's
 //              softmax has the other tile's two groups to hide behind.  S and
