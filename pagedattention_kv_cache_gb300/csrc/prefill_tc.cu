@@ -25,8 +25,9 @@
 //              O of both tiles sit in TMEM (4 x 128 columns); P is written
 //              over S in bf16 and read from TMEM as the A operand of P V.
 //   warps 2-9  softmax of tile A, two threads per TMEM lane (= query row),
-//              one per half of the key tile: scale, mask, row max (the halves
-//              exchange theirs through shared memory), exp2, bf16 P; O is
+//              one per half of the key tile: scale, mask, row max (the two
+//              warps on the same 32 rows exchange theirs through shared memory
+//              at a 64-thread named barrier), exp2, bf16 P; O is
 //              rescaled in TMEM only when the row max grows by more than 2^8;
 //              final normalisation and store (each half 64 of the 128 columns).
 //   warps 10-17  the same for tile B.
@@ -530,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = lane_addr + kColS + x * kBN;
     const uint32_t o_addr = lane_addr + kColO + x * kD + half * (kD / 2);  // this half's D / 2 output columns
     const int lim = p.causal ? min(pos, nk - 1) : nk - 1;
-    const int bar_id = 1 + x;
+    const int bar_id = 1 + x;                 // the tile's 8 softmax warps
+    const int pair_id = 3 + x * 4 + quad;     // the tile's two warps (one per half) on these 32 rows
     constexpr int kGroup = 32 * kSoftmaxWarps;
     auto red_at = [&](int parity, int h) { return red + ((parity * 2 + x) * 2 + h) * kBM + row; };
     float m_run = -INFINITY;
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx[u] = max3(mx[u], __uint_as_float(r[e + 2 * u]), __uint_as_float(r[e + 2 * u + 1]));
       }
       *red_at(j & 1, half) = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-      named_barrier_sync(bar_id, kGroup);
+      named_barrier_sync(pair_id, 64);
       const float mt = fmaxf(*red_at(j & 1, 0), *red_at(j & 1, 1));
       const float m_new = fmaxf(m_run, mt * p.scale_log2);
       const bool grow = m_new > m_run + kRescaleLog2 || (m_run == -INFINITY && m_new != -INFINITY);
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the row sum over both halves (the exchange buffers are free: every tile's
     // maxima were read before the last P_FULL)
     *red_at(0, half) = l_run;
-    named_barrier_sync(bar_id, kGroup);
+    named_barrier_sync(pair_id, 64);
     l_run = *red_at(0, 0) + *red_at(0, 1);
     // this thread's 64 outputs, 32 at a time: TMEM O (zero when the tile saw no key in this part)
     auto load_o = [&](int c, uint32_t* o) {
