@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop (its descriptor arithmetic stays warp-uniform);
     // one elected lane issues the MMAs and commits.
     {
-      const bool leader = elect_one();
+      const bool leader = tc::elect_one();
       constexpr uint32_t idesc_qk = tc::idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(kBM, kD, 0, 1);
       // descriptors of the first Q, K and V slabs; later ones differ only in the

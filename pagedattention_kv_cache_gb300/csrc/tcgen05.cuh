@@ -12,6 +12,20 @@
 namespace pkv {
 namespace tc {
 
+// ------------------------------------------------------------------ issue
+
+// True in exactly one lane of the (fully active) warp.  Code around it stays
+// warp-uniform, so values the whole warp computes can live in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------ TMEM
 
 // Allocates `ncols` (power of two, 32..512) TMEM columns; the base address is
