@@ -829,6 +829,7 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
     const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     p.parts_max = prefill_tc_parts(a.batch, a.hkv, G, a.max_seqlen_q, info.sms);
+    if (workspace_counters_ready(a.workspace, 2 * flags, stream) != PKV_OK) return PKV_ECUDA;
     p.tickets = reinterpret_cast<int*>(ws);
     p.ready = reinterpret_cast<int*>(ws + flags);
     p.records = ws + 2 * flags;

@@ -188,3 +188,25 @@ def test_repeated_calls_reuse_workspace():
         assert torch.equal(o, r["out"])
     # the workspace's ticket counters are back at zero
     assert torch.count_nonzero(ws[: 4 * w.batch]) == 0
+
+
+def test_workspace_shared_by_calls_of_growing_batch():
+    # one workspace for a small batch, then larger ones: each larger call's ticket counters lie where
+    # the previous call left partial results, and the library clears them before the launch
+    ws_calls = []
+    for seed, batch in ((61, 2), (62, 40), (63, 3), (64, 90)):
+        w = wl.random_decode(seed, batch=batch, max_ctx=4000, min_ctx=1500, block_size=16, num_q_heads=16,
+                             num_kv_heads=8, head_dim=128, dtype=torch.bfloat16)
+        t = {k: v.cuda() for k, v in wl.decode_tensors(w, "cpu").items()}
+        m = md.to_device(md.decode_metadata(w.block_tables, w.context_lens, w.block_size), "cuda")
+        ws_calls.append((w, t, m))
+    need = max(pkv.decode_workspace_bytes(w.batch, 16, 128) for w, _, _ in ws_calls)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for w, t, m in ws_calls:
+        shared = pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                                       w.scale, workspace=ws)
+        fresh = pkv.paged_decode_attn(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                                      w.scale)
+        torch.cuda.synchronize()
+        assert pkv.device_error() == 0
+        assert torch.equal(shared, fresh), w.batch

@@ -174,6 +174,34 @@ def test_long_items_split_head_dim_64():
     assert d <= 1.6e-2, d
 
 
+def test_split_workspace_shared_by_calls_of_growing_size():
+    # one workspace: a one-sequence split (few tickets, large records), then three sequences (more
+    # tickets, where the first call left records), then one again; each against the unsplit kernel
+    one = wl.random_prefill(40, batch=1, max_new=120, min_new=120, max_cached_blocks=16, block_size=256,
+                            num_q_heads=16, num_kv_heads=8, head_dim=128)
+    one.num_cached[0] = 16 * 256
+    one.block_tables[0] = list(range(-(-(16 * 256 + 120) // 256)))
+    one.num_blocks = max(one.num_blocks, len(one.block_tables[0]) + 4)
+    three = wl.random_prefill(41, batch=3, max_new=140, min_new=40, max_cached_blocks=10, block_size=256,
+                              num_q_heads=16, num_kv_heads=8, head_dim=128)
+    sizes = [pkv.prefill_workspace_bytes(w.batch, 16, 8, 128, max(w.num_new)) for w in (one, three)]
+    assert min(sizes) > 0
+    ws = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
+    for w in (one, three, one, three):
+        t = wl.prefill_tensors(w, "cuda")
+        meta = md.prefill_metadata(w.block_tables, w.num_cached, w.num_new, w.block_size, always_tables=True)
+        gm = md.to_device(meta, "cuda")
+        pkv.kv_store(t["k"], t["v"], t["k_cache"], t["v_cache"], gm["slot_mapping"])
+        outs = [pkv.paged_varlen_prefill_attn(t["q"], gm["cu_seqlens_q"], gm["cu_seqlens_k"], meta["max_seqlen_q"],
+                                              meta["max_seqlen_k"], w.scale, k_cache=t["k_cache"],
+                                              v_cache=t["v_cache"], block_tables=gm["block_tables"], workspace=ws_arg)
+                for ws_arg in (ws, False)]
+        torch.cuda.synchronize()
+        assert pkv.device_error() == 0
+        d = (outs[0].float() - outs[1].float()).abs().max().item()
+        assert d <= 1.6e-2, (w.batch, d)
+
+
 def test_single_long_history_runs_as_eight_parts():
     # one sequence, a 16k-token history and 200 new tokens: 16 pairs of query tiles for a GPU of ~150 SMs,
     # so each pair (130 key tiles of 128) runs as eight parts
