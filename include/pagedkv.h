@@ -147,14 +147,14 @@ size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int3
  *   num_splits      0 = automatic, S >= 1 = S equal parts per sequence (1 = no split)
  *   workspace       device, >= pkv_paged_decode_workspace_bytes(...) bytes, 256-byte
  *                   aligned; may be NULL when that is 0.  It must be zero-filled once
- *                   after allocation.  It starts with ticket counters that every call
- *                   leaves at zero again, then holds that call's partial results; the
- *                   library remembers, per workspace address, how much each call left
- *                   zeroed, and before a call that needs more counters (a larger batch)
- *                   it clears the difference on `stream` (cudaMemsetAsync).  So calls of
- *                   any sizes may share it.  A call that raised PKV_DERR_WAIT_TIMEOUT may
- *                   leave counters set: zero the workspace again after one.  Calls
- *                   sharing a workspace must not overlap in time.
+ *                   after allocation.  Its first 64 KiB hold ticket counters only, which
+ *                   every call leaves at zero again; partial results follow them.  So
+ *                   calls of any sizes, eager or replayed from CUDA graphs, may share it
+ *                   (and share it with pkv_paged_varlen_prefill_attn, whose workspace
+ *                   starts with the same counter area); only batches whose batch + parts
+ *                   exceed 16,384 counters extend the area.  A call that raised
+ *                   PKV_DERR_WAIT_TIMEOUT may leave counters set: zero the workspace again
+ *                   after one.  Calls sharing a workspace must not overlap in time.
  * Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; num_kv_heads in [1, 8];
  * dtype F32 or BF16.
  */
@@ -322,9 +322,9 @@ int pkv_paged_decode_attn_noalloc(void* out, const void* q, const void* k_cache,
  *                   P = min(8, SMs / pairs) parts over consecutive key ranges
  *                   and merges them (log-sum-exp, in part order, so results do not depend
  *                   on timing).  Otherwise nothing is split.  It must be zero-filled once
- *                   after allocation; its tickets are kept as for pkv_paged_decode_attn's
- *                   workspace (calls of any sizes may share it).  Calls sharing a
- *                   workspace must not overlap in time.
+ *                   after allocation; its first 64 KiB are the same counter area as in
+ *                   pkv_paged_decode_attn's workspace (calls of any sizes may share it).
+ *                   Calls sharing a workspace must not overlap in time.
  * Supported: BF16 only; head_dim 64 or 128; G in {1, 2, 4, 8}.  Block sizes that
  * are a multiple of 128, or a divisor of 128 of at least 8, and the packed path run
  * on the tcgen05 tensor-core kernel; other block sizes on an mma.sync kernel (which
@@ -345,9 +345,11 @@ int pkv_paged_varlen_prefill_attn(void* out, const void* q, const void* k, const
 /*
  * Bytes of the optional workspace of pkv_paged_varlen_prefill_attn for these
  * sizes on the current device: a ticket and a ready count per (sequence, KV
- * head, query tile; the tiles rounded up to whole pairs), each array padded to
- * 256 bytes, then P records of 66,560 bytes per query tile, P as above.  0 when nothing would be split (the items fill
- * the GPU, the shape has no tensor-core path, or no device is present).  This
+ * head, query tile; the tiles rounded up to whole pairs), each array in one
+ * 32 KiB half of the 64 KiB counter area, then P records of 66,560 bytes
+ * (head_dim 128; 33,792 for 64) per query tile, P as above.  0 when nothing
+ * would be split (the items fill the GPU, the shape has no tensor-core path,
+ * or no device is present).  This
  * sizing rule is the library's own (the pages' flash-attn call has no
  * workspace); it follows the split-decode workspace above.
  */

@@ -2,9 +2,7 @@
 // the per-device error word the kernels raise bits in.
 #include <cuda.h>
 
-#include <cstdint>
 #include <mutex>
-#include <unordered_map>
 
 #include "common.cuh"
 
@@ -42,26 +40,9 @@ int prepare_slot(DeviceSlot** out) {
   return PKV_OK;
 }
 
-// Per workspace address: the leading bytes the last call on it left zeroed.
-std::mutex g_ws_mutex;
-std::unordered_map<uintptr_t, size_t> g_ws_zeroed;
-
 }  // namespace
 
 namespace pkv {
-
-int workspace_counters_ready(void* workspace, size_t counter_bytes, cudaStream_t stream) {
-  const uintptr_t key = reinterpret_cast<uintptr_t>(workspace);
-  std::lock_guard<std::mutex> lock(g_ws_mutex);
-  const auto it = g_ws_zeroed.find(key);
-  const size_t zeroed = it == g_ws_zeroed.end() ? SIZE_MAX : it->second;
-  if (counter_bytes > zeroed &&
-      cudaMemsetAsync(static_cast<unsigned char*>(workspace) + zeroed, 0, counter_bytes - zeroed, stream) !=
-          cudaSuccess)
-    return PKV_ECUDA;
-  g_ws_zeroed[key] = counter_bytes;  // the call resets its counters; its records fill what follows
-  return PKV_OK;
-}
 
 int device_info(DeviceInfo* info) {
   DeviceSlot* s = nullptr;

@@ -25,14 +25,12 @@ struct DeviceInfo {
 };
 int device_info(DeviceInfo* info);            // returns PKV_OK or PKV_ECUDA
 unsigned int* device_error_word(int* status);  // device address of this device's error word
-// Split workspaces (decode and prefill) start with ticket counters that each
-// call leaves at zero again; its records follow them.  A later call whose
-// counter region is larger would find records there, so before a launch this
-// clears, on `stream`, the part of [0, counter_bytes) that the previous call
-// on the same workspace address did not leave zeroed (nothing in the steady
-// state).  A workspace address seen for the first time is taken as
-// zero-filled, as the callers are told to provide it.
-int workspace_counters_ready(void* workspace, size_t counter_bytes, cudaStream_t stream);
+// Split workspaces (decode and prefill) start with a counter area of this size
+// for every call: ticket counters, which each call leaves at zero again, and
+// nothing else.  Partial results follow it, so no call's results ever lie
+// where another call's counters are, whatever the two calls' sizes and
+// whether they run eagerly or are replayed from a CUDA graph.
+constexpr size_t kWorkspaceCounterBytes = 64 * 1024;
 
 // Encodes a 3-D bf16 tensor map (dims innermost first, rows of d0 contiguous
 // elements) with 128-byte swizzle for tiled TMA loads of box b0 x b1 x b2.

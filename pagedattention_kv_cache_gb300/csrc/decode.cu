@@ -85,7 +85,6 @@ extern "C" int pkv_paged_decode_attn(void* out, const void* q, const void* k_cac
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return PKV_EWORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_EALIGN;
-    if (pkv::workspace_counters_ready(workspace, off_o, stream) != PKV_OK) return PKV_ECUDA;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     p.counters = reinterpret_cast<int32_t*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + off_o);

@@ -38,6 +38,8 @@
 // points that include it are decode.cu, verify.cu and fp8.cu.
 #pragma once
 
+#include <algorithm>
+
 #include "decode_mma.cuh"
 #include "decode_simt.cuh"
 
@@ -77,8 +79,10 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 size_t workspace_layout(int batch, int hq, int d, int num_splits, int sms, size_t* off_o, size_t* off_ml) {
   const size_t slots = slot_count(batch, num_splits, sms);
   if (slots == 0) return 0;
-  // tickets: one per sequence, then one per slot (the merge groups)
-  const size_t counters = align256((static_cast<size_t>(batch) + slots) * sizeof(int32_t));
+  // tickets: one per sequence, then one per slot (the merge groups), in the
+  // fixed counter area (larger only past 16,384 counters)
+  const size_t counters =
+      std::max(pkv::kWorkspaceCounterBytes, align256((static_cast<size_t>(batch) + slots) * sizeof(int32_t)));
   *off_o = counters;
   *off_ml = counters + align256(slots * hq * d * sizeof(float));
   return *off_ml + align256(slots * hq * 2 * sizeof(float));

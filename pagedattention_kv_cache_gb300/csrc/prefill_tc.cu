@@ -152,8 +152,15 @@ int prefill_tc_parts(int batch, int num_kv_heads, int group, int max_seqlen_q, i
   return static_cast<int>(std::min<long long>(kMaxParts, sms / pairs));
 }
 
-// Workspace of the tcgen05 prefill: tickets and ready counts (256-byte aligned
-// blocks), then P records per (sequence, KV head, query tile); 0 when the
+// Bytes of each of the two int arrays (tickets, ready counts) at the start of
+// the prefill workspace: a half of the fixed counter area (split launches have
+// at most one item per SM, far below its 8,192 counters), more only past it.
+size_t prefill_tc_flag_bytes(long long items) {
+  return std::max(kWorkspaceCounterBytes / 2, static_cast<size_t>((items * 4 + 255) / 256 * 256));
+}
+
+// Workspace of the tcgen05 prefill: tickets and ready counts (the counter
+// area), then P records per (sequence, KV head, query tile); 0 when the
 // current device's SMs are filled without splitting.
 size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int head_dim, int max_seqlen_q) {
   if (batch <= 0 || num_kv_heads <= 0 || max_seqlen_q <= 0) return 0;
@@ -165,7 +172,7 @@ size_t prefill_tc_workspace_bytes(int batch, int num_kv_heads, int group, int he
   if (parts == 1) return 0;
   const long long tq = kBM / group;
   const long long items = static_cast<long long>(batch) * num_kv_heads * 2 * ((max_seqlen_q + 2 * tq - 1) / (2 * tq));
-  const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
+  const size_t flags = prefill_tc_flag_bytes(items);
   const size_t record = head_dim == 64 ? Geo<64>::kRecordBytes : Geo<128>::kRecordBytes;
   return 2 * flags + static_cast<size_t>(items) * parts * record;
 }
@@ -826,10 +833,9 @@ int launch(const PrefillArgs& a, cudaStream_t stream) {
   const size_t ws_need = prefill_tc_workspace_bytes(a.batch, a.hkv, G, D, a.max_seqlen_q);
   if (a.workspace && ws_need > 0 && a.workspace_bytes >= ws_need) {
     const long long items = static_cast<long long>(a.batch) * a.hkv * p.q_tiles;
-    const size_t flags = static_cast<size_t>((items * 4 + 255) / 256 * 256);
+    const size_t flags = prefill_tc_flag_bytes(items);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     p.parts_max = prefill_tc_parts(a.batch, a.hkv, G, a.max_seqlen_q, info.sms);
-    if (workspace_counters_ready(a.workspace, 2 * flags, stream) != PKV_OK) return PKV_ECUDA;
     p.tickets = reinterpret_cast<int*>(ws);
     p.ready = reinterpret_cast<int*>(ws + flags);
     p.records = ws + 2 * flags;

@@ -62,8 +62,8 @@ def test_prefill_workspace_is_zero_when_nothing_splits():
 def test_prefill_workspace_size_rule():
     # work items are pairs of query tiles of 128 / G tokens, one CTA per SM: P = floor(SMs / pairs) parts
     # (at most 8, one wave) when at most half the SMs have a pair; then one int ticket and one int ready
-    # count per (sequence, KV head, query tile), each array padded to 256 bytes, and P records of
-    # 128 rows x (128 fp32 + m + l) per query tile
+    # count per (sequence, KV head, query tile), each array in a 32 KiB half of the 64 KiB counter
+    # area, and P records of 128 rows x (128 fp32 + m + l) per query tile
     lib = _lib.load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
@@ -74,7 +74,7 @@ def test_prefill_workspace_size_rule():
             return 0
         parts = min(8, sms // pairs)
         items = 2 * pairs
-        flags = -(-items * 4 // 256) * 256
+        flags = max(32768, -(-items * 4 // 256) * 256)
         return 2 * flags + items * parts * (128 * 128 * 4 + 128 * 8)
 
     for batch, hq, hkv, max_q in [(16, 16, 8, 512), (1, 8, 8, 1), (3, 32, 4, 1000), (1, 16, 8, 512), (2, 32, 8, 300)]:

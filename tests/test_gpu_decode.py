@@ -191,8 +191,8 @@ def test_repeated_calls_reuse_workspace():
 
 
 def test_workspace_shared_by_calls_of_growing_batch():
-    # one workspace for a small batch, then larger ones: each larger call's ticket counters lie where
-    # the previous call left partial results, and the library clears them before the launch
+    # one workspace for a small batch, then larger ones: every call's ticket counters sit in the fixed
+    # counter area at the start, which no call's partial results reach
     ws_calls = []
     for seed, batch in ((61, 2), (62, 40), (63, 3), (64, 90)):
         w = wl.random_decode(seed, batch=batch, max_ctx=4000, min_ctx=1500, block_size=16, num_q_heads=16,
