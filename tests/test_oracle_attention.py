@@ -245,6 +245,28 @@ def test_prefill_no_history_packed_path():
             np.testing.assert_allclose(out[sl, h], ref, rtol=1e-12, atol=1e-12)
 
 
+def test_prefill_non_causal_matches_textbook_full():
+    # causal=False: every query row of a sequence attends all nk keys, history and new alike
+    rng = np.random.default_rng(22)
+    cached = [0, 4, 9]
+    new = [6, 3, 2]
+    full = [c + n for c, n in zip(cached, new)]
+    kc, vc, bt, ks, vs = _place(rng, full, 4, 2, 8)
+    q = rng.standard_normal((sum(new), 4, 8))
+    cu_q = np.concatenate([[0], np.cumsum(new)])
+    cu_k = np.concatenate([[0], np.cumsum(full)])
+    paged = oa.paged_prefill_attention(q, cu_q, cu_k, 0.3, k_cache=kc, v_cache=vc, block_tables=bt, causal=False)
+    k_packed = np.concatenate(ks)
+    v_packed = np.concatenate(vs)
+    packed = oa.paged_prefill_attention(q, cu_q, cu_k, 0.3, k=k_packed, v=v_packed, causal=False)
+    for i in range(3):
+        rows = slice(cu_q[i], cu_q[i + 1])
+        for h in range(4):
+            ref = _textbook(q[rows, h], ks[i][:, h // 2], vs[i][:, h // 2], 0.3)
+            np.testing.assert_allclose(paged[rows, h], ref, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(packed[rows, h], ref, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------ invariants
 
 def test_block_permutation_invariance():

@@ -43,6 +43,7 @@ MUTANTS = {
     "causal_top_left": ("attention", "visible = cols <= cached + rows", "visible = cols <= rows"),
     "causal_strict": ("attention", "visible = cols <= cached + rows", "visible = cols < cached + rows"),
     "history_short_by_one": ("attention", "cached = nk - nq", "cached = nk - nq - 1"),
+    "non_causal_still_masked": ("attention", "if causal:", "if True:"),
     "combine_l_unweighted": ("attention", "total_l = sum(w[j] * parts[j][2]", "total_l = sum(parts[j][2]"),
     "combine_weights_inverted": ("attention", "w = np.exp(ms - big_m)", "w = np.exp(big_m - ms)"),
     "partial_o_normalised": ("attention", "o[h] = p @ values[lo:hi, g]", "o[h] = p @ values[lo:hi, g] / p.sum()"),
