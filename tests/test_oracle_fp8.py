@@ -70,3 +70,34 @@ def test_quantize_rounds_the_float32_quotient():
             assert fp8.quantize(x, float(s)) == want
             found += 1
     assert found >= 10
+
+
+def test_kv_store_fp8_closed_form():
+    # each token's K and V rows land, quantized with their own scale, at (block, offset) found by
+    # walking the pool block by block; slot -1 and every other byte are left as they were
+    rng = np.random.default_rng(7)
+    num_blocks, bs, hkv, d = 6, 4, 2, 8
+    k_cache = rng.integers(0, 256, (num_blocks, bs, hkv, d), dtype=np.uint8)
+    v_cache = rng.integers(0, 256, (num_blocks, bs, hkv, d), dtype=np.uint8)
+    slots = [9, -1, 0, 23, 14]
+    k = (rng.standard_normal((len(slots), hkv, d)) * 3).astype(np.float32)
+    v = (rng.standard_normal((len(slots), hkv, d)) * 3).astype(np.float32)
+    k_scale, v_scale = 0.05, 0.02
+    k_out, v_out = fp8.kv_store_fp8(k_cache, v_cache, k, v, slots, k_scale, v_scale)
+    want_k, want_v = k_cache.copy(), v_cache.copy()
+    def code(x, scale):  # float32 quotient, saturated at the largest finite value, then torch's conversion
+        quot = min(max(float(np.float32(x) / np.float32(scale)), -448.0), 448.0)
+        return torch.tensor(quot).to(torch.float8_e4m3fn).view(torch.uint8).item()
+
+    flat = 0
+    for blk in range(num_blocks):
+        for off in range(bs):
+            if flat in slots:
+                i = slots.index(flat)
+                want_k[blk, off] = [[code(x, k_scale) for x in row] for row in k[i]]
+                want_v[blk, off] = [[code(x, v_scale) for x in row] for row in v[i]]
+            flat += 1
+    assert np.array_equal(k_out, want_k)
+    assert np.array_equal(v_out, want_v)
+    with pytest.raises(IndexError):
+        fp8.kv_store_fp8(k_cache, v_cache, k[:1], v[:1], [num_blocks * bs], k_scale, v_scale)

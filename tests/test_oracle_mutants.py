@@ -71,6 +71,8 @@ MUTANTS = {
     "ties_not_to_even": ("fp8", "((d_hi == d_lo) & (_POS_CODES[hi] % 2 == 0) & (hi != lo))",
                          "((d_hi == d_lo) & (hi != lo))"),
     "sign_dropped": ("fp8", "code = np.where(neg, code | 0x80, code)", "code = np.where(neg, code, code)"),
+    "fp8_store_v_with_k_scale": ("fp8", "quantize(v[i], v_scale)", "quantize(v[i], k_scale)"),
+    "fp8_store_block_offset_swapped": ("fp8", "blk, off = divmod(slot, bs)", "off, blk = divmod(slot, bs)"),
     "quantize_divides_in_float64": ("fp8", "q = np.asarray(x, dtype=np.float32) / np.float32(scale)",
                                     "q = np.asarray(x, dtype=np.float64) / float(scale)"),
 }
