@@ -44,6 +44,7 @@ MUTANTS = {
     "causal_strict": ("attention", "visible = cols <= cached + rows", "visible = cols < cached + rows"),
     "history_short_by_one": ("attention", "cached = nk - nq", "cached = nk - nq - 1"),
     "non_causal_still_masked": ("attention", "if causal:", "if True:"),
+    "packed_keys_at_query_offsets": ("attention", "keys = _f64(k[k0:k1])", "keys = _f64(k[q0:q0 + nk])"),
     "combine_l_unweighted": ("attention", "total_l = sum(w[j] * parts[j][2]", "total_l = sum(parts[j][2]"),
     "combine_weights_inverted": ("attention", "w = np.exp(ms - big_m)", "w = np.exp(big_m - ms)"),
     "partial_o_normalised": ("attention", "o[h] = p @ values[lo:hi, g]", "o[h] = p @ values[lo:hi, g] / p.sum()"),
